@@ -1,0 +1,311 @@
+"""Python binding of the GB300 dense GEMM library (D = A @ B^T, fp32 accumulation).
+
+Argument marshalling only: every step of the product runs in the CUDA library
+``libdgb_gemm.so`` (built by :func:`build`).  The functions keep the names of
+the C ABI in ``include/gemm.h``; :class:`Plan` and :func:`matmul` wrap them for
+torch CUDA tensors and the current torch stream.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from ._build import LIB as _LIB_PATH, build as _build
+
+__all__ = [
+    "build", "lib", "GemmError", "GemmDesc", "GemmPlanInfo", "GemmDeviceProps", "GemmDeviceError",
+    "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host",
+    "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
+    "gemm_version", "Plan", "matmul", "header_functions",
+]
+
+# ---------------------------------------------------------------- constants (include/gemm.h)
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT = 0, 1, 2, 3
+GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE, GEMM_ERR_RESOURCES = 4, 5, 6, 7
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32 = 0, 1, 2, 3
+GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
+GEMM_SCALE_NONE, GEMM_SCALE_BLOCK_1x128_128x128 = 0, 1
+GEMM_KERNEL_SINGLE_CTA, GEMM_KERNEL_PERSISTENT, GEMM_KERNEL_FP8_BLOCK, GEMM_KERNEL_ZERO_FILL = 1, 2, 3, 4
+GEMM_FLAG_CTA_GROUP_1 = 1 << 0
+GEMM_FLAG_CTA_GROUP_2 = 1 << 1
+GEMM_FLAG_NO_SINGLE_CTA = 1 << 2
+GEMM_FLAG_SINGLE_CTA = 1 << 3
+GEMM_FLAG_TEST_DROP_LOAD = 1 << 30
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+
+
+class GemmDesc(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("batch", ctypes.c_int64),
+        ("dtype_a", ctypes.c_int32), ("dtype_b", ctypes.c_int32), ("dtype_d", ctypes.c_int32),
+        ("major_a", ctypes.c_int32), ("major_b", ctypes.c_int32), ("scale_mode", ctypes.c_int32),
+        ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64),
+        ("stride_a", ctypes.c_int64), ("stride_b", ctypes.c_int64), ("stride_d", ctypes.c_int64),
+        ("ld_sa", ctypes.c_int64), ("ld_sb", ctypes.c_int64),
+        ("stride_sa", ctypes.c_int64), ("stride_sb", ctypes.c_int64),
+        ("flags", ctypes.c_uint32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
+        ("max_ctas", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_uint64),
+    ]
+
+
+class GemmPlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int32), ("cta_group", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+        ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+        ("tmem_stages", ctypes.c_int32), ("tmem_cols", ctypes.c_int32), ("grid", ctypes.c_int32),
+        ("block_threads", ctypes.c_int32), ("num_tiles", ctypes.c_int64), ("stage_bytes", ctypes.c_int64),
+        ("pipeline_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemmDeviceProps(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int32), ("smem_optin_bytes", ctypes.c_int32),
+                ("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32)]
+
+
+class GemmDeviceError(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_uint32), ("role", ctypes.c_uint32), ("stage", ctypes.c_uint32),
+                ("tile", ctypes.c_uint32), ("block", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 3)]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = int(status)
+        msg = gemm_status_string(status) if _lib is not None else str(status)
+        if self.status == GEMM_ERR_CUDA and _lib is not None:
+            msg += " (cudaError %d)" % gemm_last_cuda_error()
+        super().__init__("%s: %s" % (where, msg) if where else msg)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    return _build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(_LIB_PATH):
+                    raise RuntimeError("CUDA library %s is missing: call dense_gemm_blackwell_gb300.build()"
+                                       % _LIB_PATH)
+                L = ctypes.CDLL(_LIB_PATH)
+                vp, st = ctypes.c_void_p, ctypes.c_int
+                L.gemm_plan_query.argtypes = [ctypes.POINTER(GemmDesc), ctypes.POINTER(GemmDeviceProps),
+                                              ctypes.POINTER(GemmPlanInfo)]
+                L.gemm_plan_query.restype = st
+                L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(GemmDesc)]
+                L.gemm_plan_create.restype = st
+                L.gemm_plan_info.argtypes = [vp, ctypes.POINTER(GemmPlanInfo)]
+                L.gemm_plan_info.restype = st
+                L.gemm_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+                L.gemm_run.restype = st
+                L.gemm_run_host.argtypes = [vp] * 12
+                L.gemm_run_host.restype = st
+                L.gemm_sync_status.argtypes = [vp, vp, ctypes.POINTER(GemmDeviceError)]
+                L.gemm_sync_status.restype = st
+                L.gemm_plan_destroy.argtypes = [vp]
+                L.gemm_plan_destroy.restype = st
+                L.gemm_status_string.argtypes = [st]
+                L.gemm_status_string.restype = ctypes.c_char_p
+                L.gemm_last_cuda_error.restype = st
+                L.gemm_version.restype = st
+                _lib = L
+    return _lib
+
+
+def header_functions():
+    """Names of the functions include/gemm.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(gemm_\w+)\s*\(", text, re.M)))
+
+
+# ---------------------------------------------------------------- C ABI, same names
+
+def gemm_plan_query(desc: GemmDesc, props: GemmDeviceProps):
+    info = GemmPlanInfo()
+    s = lib().gemm_plan_query(ctypes.byref(desc), ctypes.byref(props), ctypes.byref(info))
+    return s, info
+
+
+def gemm_plan_create(desc: GemmDesc):
+    h = ctypes.c_void_p()
+    s = lib().gemm_plan_create(ctypes.byref(h), ctypes.byref(desc))
+    if s != GEMM_OK:
+        raise GemmError(s, "gemm_plan_create")
+    return h
+
+
+def gemm_plan_info(plan) -> GemmPlanInfo:
+    info = GemmPlanInfo()
+    s = lib().gemm_plan_info(plan, ctypes.byref(info))
+    if s != GEMM_OK:
+        raise GemmError(s, "gemm_plan_info")
+    return info
+
+
+def gemm_run(plan, A, B, D, scale_a=None, scale_b=None, stream=None) -> int:
+    return lib().gemm_run(plan, A, B, D, scale_a, scale_b, stream)
+
+
+def gemm_run_host(plan, hA, hB, hD, hsa, hsb, dA, dB, dD, dsa, dsb, stream=None) -> int:
+    return lib().gemm_run_host(plan, hA, hB, hD, hsa, hsb, dA, dB, dD, dsa, dsb, stream)
+
+
+def gemm_sync_status(plan, stream=None):
+    rec = GemmDeviceError()
+    s = lib().gemm_sync_status(plan, stream, ctypes.byref(rec))
+    return s, rec
+
+
+def gemm_plan_destroy(plan) -> int:
+    return lib().gemm_plan_destroy(plan)
+
+
+def gemm_status_string(status) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+def gemm_last_cuda_error() -> int:
+    return lib().gemm_last_cuda_error()
+
+
+def gemm_version() -> int:
+    return lib().gemm_version()
+
+
+# ---------------------------------------------------------------- torch convenience
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32,
+             torch.float8_e4m3fn: GEMM_E4M3}
+    if t not in codes:
+        raise TypeError("unsupported dtype %s" % t)
+    return codes[t]
+
+
+def _torch_dtype(code):
+    import torch
+    return {GEMM_F16: torch.float16, GEMM_BF16: torch.bfloat16, GEMM_F32: torch.float32,
+            GEMM_E4M3: torch.float8_e4m3fn}[code]
+
+
+def make_desc(M, N, K, *, batch=1, dtype_a=GEMM_BF16, dtype_b=None, dtype_d=GEMM_F32,
+              major_a=GEMM_K_MAJOR, major_b=GEMM_K_MAJOR, scale_mode=GEMM_SCALE_NONE,
+              lda=0, ldb=0, ldd=0, stride_a=0, stride_b=0, stride_d=0, ld_sa=0, ld_sb=0,
+              stride_sa=0, stride_sb=0, flags=0, tile_n=0, stages=0, max_ctas=0, wait_timeout_ns=0) -> GemmDesc:
+    d = GemmDesc()
+    d.M, d.N, d.K, d.batch = M, N, K, batch
+    d.dtype_a = dtype_a
+    d.dtype_b = dtype_a if dtype_b is None else dtype_b
+    d.dtype_d = dtype_d
+    d.major_a, d.major_b, d.scale_mode = major_a, major_b, scale_mode
+    d.lda, d.ldb, d.ldd = lda, ldb, ldd
+    d.stride_a, d.stride_b, d.stride_d = stride_a, stride_b, stride_d
+    d.ld_sa, d.ld_sb, d.stride_sa, d.stride_sb = ld_sa, ld_sb, stride_sa, stride_sb
+    d.flags, d.tile_n, d.stages, d.max_ctas = flags, tile_n, stages, max_ctas
+    d.wait_timeout_ns = wait_timeout_ns
+    return d
+
+
+class Plan:
+    """A created plan (owns the C handle); use as a context manager or call close()."""
+
+    def __init__(self, desc: GemmDesc):
+        self.desc = desc
+        self.handle = gemm_plan_create(desc)
+        self.info = gemm_plan_info(self.handle)
+
+    def run(self, A, B, D, scale_a=None, scale_b=None, stream=None):
+        """Enqueue on `stream` (default: torch's current stream); tensors are torch CUDA tensors."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        s = gemm_run(self.handle, ptr(A), ptr(B), ptr(D), ptr(scale_a), ptr(scale_b), stream)
+        if s != GEMM_OK:
+            raise GemmError(s, "gemm_run")
+
+    def run_host(self, hA, hB, hD, dA, dB, dD, hsa=None, hsb=None, dsa=None, dsb=None, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        s = gemm_run_host(self.handle, ptr(hA), ptr(hB), ptr(hD), ptr(hsa), ptr(hsb), ptr(dA), ptr(dB),
+                          ptr(dD), ptr(dsa), ptr(dsb), stream)
+        if s != GEMM_OK:
+            raise GemmError(s, "gemm_run_host")
+
+    def sync_status(self, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        return gemm_sync_status(self.handle, stream)
+
+    def close(self):
+        if self.handle is not None:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_plan_cache = {}
+
+
+def matmul(a, b, *, out=None, out_dtype=None, scale_a=None, scale_b=None, flags=0, tile_n=0, stages=0):
+    """D = a @ b^T for torch CUDA tensors.
+
+    a: [M, K] or [batch, M, K] (last dim contiguous), b: [N, K] or [batch, N, K];
+    e4m3 inputs need scale_a [M, ceil(K/128)] and scale_b [ceil(N/128), ceil(K/128)] fp32.
+    Returns D [M, N] / [batch, M, N] in out_dtype (default fp32).
+    """
+    import torch
+    batched = a.dim() == 3
+    if batched:
+        batch, M, K = a.shape
+        N = b.shape[1]
+    else:
+        batch, (M, K), N = 1, a.shape, b.shape[0]
+    if a.stride(-1) != 1 or b.stride(-1) != 1:
+        raise ValueError("inputs must be K-contiguous")
+    code_d = _dtype_code(out_dtype or (out.dtype if out is not None else torch.float32))
+    if out is None:
+        shape = (batch, M, N) if batched else (M, N)
+        out = torch.empty(shape, dtype=_torch_dtype(code_d), device=a.device)
+    da = _dtype_code(a.dtype)
+    desc = make_desc(M, N, K, batch=batch, dtype_a=da, dtype_b=_dtype_code(b.dtype), dtype_d=code_d,
+                     scale_mode=GEMM_SCALE_BLOCK_1x128_128x128 if da == GEMM_E4M3 else GEMM_SCALE_NONE,
+                     lda=a.stride(-2), ldb=b.stride(-2), ldd=out.stride(-2),
+                     stride_a=a.stride(0) if batched else 0, stride_b=b.stride(0) if batched else 0,
+                     stride_d=out.stride(0) if batched else 0, flags=flags, tile_n=tile_n, stages=stages)
+    key = (a.device.index, bytes(desc))
+    plan = _plan_cache.get(key)
+    if plan is None:
+        plan = _plan_cache[key] = Plan(desc)
+    plan.run(a, b, out, scale_a, scale_b)
+    return out

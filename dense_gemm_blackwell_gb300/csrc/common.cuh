@@ -1,0 +1,143 @@
+// common.cuh -- descriptors, launch parameters and bounded waits shared by the
+// GEMM kernels (host and device).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace dgb {
+
+// ---------------------------------------------------------------- descriptors
+//
+// Shared-memory matrix descriptor for tcgen05.mma (public PTX ISA, "Shared
+// memory descriptor"; the pages do not print its bits):
+//   [0,14)  start address >> 4         [16,30) leading-dim byte offset >> 4
+//   [32,46) stride-dim byte offset >> 4 [46,48) version = 1
+//   [49,52) base offset                 [52]    LBO mode (0 = relative)
+//   [61,64) swizzle: 0 none, 1 128B/32B-atom, 2 128B, 4 64B, 6 32B
+//
+// Operand tiles are K-major with the 128-byte swizzle (TVM TIRx "Blackwell
+// Tensor Cores": swizzle mode 3 = 128 B, 1024-byte period, hence 1024-byte
+// tile alignment).  Each row of a tile is 128 bytes of K; eight rows form one
+// 1024-byte swizzle atom, so the stride between 8-row groups is 1024 bytes.
+// The leading-dim offset is unused when one MMA's K (32 bytes) lies inside
+// the 128-byte swizzle row.  Advancing K by 32 bytes inside the row is a +2
+// on the start-address field: the swizzle is applied to absolute address
+// bits, so a 1024-aligned tile keeps matching what TMA wrote.
+constexpr uint64_t kSmemDescSw128KMajorBase =
+    (uint64_t(1) << 16) |            // LBO (unused), 16 bytes
+    (uint64_t(1024 >> 4) << 32) |    // SBO: 8 rows x 128 B
+    (uint64_t(1) << 46) |            // descriptor version for tcgen05
+    (uint64_t(2) << 61);             // 128-byte swizzle
+
+__host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t smem_addr) {
+    return kSmemDescSw128KMajorBase | uint64_t((smem_addr >> 4) & 0x3FFFu);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 / kind::f8f6f4 (public PTX ISA):
+//   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
+//   [15] A major (0 = K)       [16] B major      [17,23) N >> 3   [24,29) M >> 4
+// A/B format for kind::f16: 0 = f16, 1 = bf16; for kind::f8f6f4: 0 = e4m3.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m, uint32_t n,
+                                                  uint32_t a_mn_major = 0, uint32_t b_mn_major = 0) {
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn_major << 15) |
+           (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- parameters
+
+enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleSingle = 4 };
+
+// Persistent warp-specialised kernel: one CTA (or CTA pair) per SM, loops over
+// output tiles.  Passed by value as a __grid_constant__ parameter.
+struct PersistentParams {
+    CUtensorMap tmap_a;   // A: (K, M[, batch]) box (tile_k, 128[, 1])
+    CUtensorMap tmap_b;   // B: (K, N[, batch]) box (tile_k, tile_n / cta_group[, 1])
+    CUtensorMap tmap_d;   // D: (N, M[, batch]) box (128 B of columns, 32[, 1])
+    gemm_device_error_t* status;
+    const float* scale_a; // block-scaled kernels only
+    const float* scale_b;
+    int64_t ld_sa, ld_sb;
+    int32_t M, N, K, batch;
+    int32_t num_m_blocks, num_n_blocks, num_k_blocks;
+    int32_t tiles_per_batch, num_tiles;
+    int32_t tile_n, stages, tmem_cols, tmem_stages;
+    int32_t group_m;
+    int32_t batched;          // 1 = 3-D tensor maps
+    uint32_t idesc;
+    uint32_t stage_bytes_a;   // per CTA
+    uint32_t stage_bytes_b;   // per CTA
+    uint32_t flags;
+    uint64_t timeout_ns;
+};
+
+// Single-CTA kernel: one CTA per batch entry, threads stage the operands.
+struct SingleParams {
+    const void* A;
+    const void* B;
+    void* D;
+    gemm_device_error_t* status;
+    int64_t lda, ldb, ldd, stride_a, stride_b, stride_d;
+    int32_t M, N, K;
+    int32_t n_pad, k_pad;     // N rounded up to 16, K rounded up to 64
+    int32_t major_a, major_b;
+    int32_t tmem_cols;
+    uint32_t idesc;
+    uint64_t timeout_ns;
+};
+
+// ---------------------------------------------------------------- bounded waits
+
+// Record the first device-side timeout of a launch in the plan's status record.
+__device__ __forceinline__ void report_timeout(gemm_device_error_t* st, uint32_t role,
+                                               uint32_t stage, uint32_t tile) {
+    if (st == nullptr) return;
+    if (atomicCAS(&st->code, 0u, (uint32_t)GEMM_ERR_TIMEOUT) == 0u) {
+        st->role = role;
+        st->stage = stage;
+        st->tile = tile;
+        st->block = blockIdx.x;
+        __threadfence();
+    }
+}
+
+// Bounded wait on an mbarrier phase.  Returns true when the phase completed,
+// false when the CTA's abort flag was raised or `timeout_ns` elapsed (the
+// timeout is recorded and the abort flag raised).  Callers leave their loops
+// on false; every wait in the kernels goes through this function.
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                           uint64_t timeout_ns, gemm_device_error_t* st,
+                                           uint32_t role, uint32_t stage, uint32_t tile) {
+    auto probe = [&]() {
+        return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (probe()) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            report_timeout(st, role, stage, tile);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+// Wait that ignores the abort flag (used while draining in-flight copies on
+// the abort path); bounded by `timeout_ns`, result not reported.
+__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+}  // namespace dgb

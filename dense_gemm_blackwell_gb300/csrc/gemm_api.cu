@@ -1,0 +1,509 @@
+// gemm_api.cu -- the C ABI declared in include/gemm.h: planner, TMA tensor-map
+// builder, launches and status reporting.  Host code only.
+//
+// Planner gates (cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", section
+// "Descriptor" and "Depth and shared memory"):
+//   * 16-bit inputs (f16 x f16 or bf16 x bf16) with f32 accumulation; 8-bit
+//     e4m3 x e4m3 only with block scales;
+//   * one MMA tile is 128 rows per SM (256 for an SM pair) by tile_n columns,
+//     tile_n a multiple of 16 up to 256, and its fp32 accumulator (tile_n
+//     32-bit columns, two buffers) must fit the 512 tensor-memory columns;
+//   * 16-byte alignment of A, B and D;
+//   * ring depth = the largest that fits the opt-in shared-memory limit, where
+//     one stage holds one A and one B tile, (M*K + N*K) * sizeof(input), and
+//     each barrier costs 8 bytes (two per stage, two per TMEM stage) plus a
+//     4-byte tensor-memory handle.
+// Unsupported requests fail with GEMM_ERR_UNSUPPORTED instead of running
+// another path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using dgb::PersistentParams;
+using dgb::SingleParams;
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kPersistentThreads = 192;
+constexpr int64_t kStagingBytes = 4 * 2 * 32 * 128;   // 4 epilogue warps x 2 buffers x 4 KB
+constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
+
+thread_local int g_last_cuda_error = 0;
+
+gemm_status_t cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return GEMM_ERR_CUDA;
+}
+
+int elem_bytes(int dt) {
+    switch (dt) {
+    case GEMM_F16: case GEMM_BF16: return 2;
+    case GEMM_E4M3: return 1;
+    case GEMM_F32: return 4;
+    default: return 0;
+    }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+int pow2_at_least(int64_t x) {
+    int v = 32;
+    while (v < x) v <<= 1;
+    return v;
+}
+
+// Descriptor with every optional field resolved to its documented default.
+struct Resolved {
+    gemm_desc_t d;
+};
+
+gemm_status_t resolve(const gemm_desc_t* in, Resolved* out) {
+    if (!in || !out) return GEMM_ERR_INVALID_ARG;
+    gemm_desc_t d = *in;
+    if (d.M < 0 || d.N < 0 || d.K < 0 || d.batch < 0) return GEMM_ERR_INVALID_ARG;
+    if (elem_bytes(d.dtype_a) == 0 || elem_bytes(d.dtype_b) == 0 || elem_bytes(d.dtype_d) == 0)
+        return GEMM_ERR_INVALID_ARG;
+    if ((d.major_a != GEMM_K_MAJOR && d.major_a != GEMM_MN_MAJOR) ||
+        (d.major_b != GEMM_K_MAJOR && d.major_b != GEMM_MN_MAJOR))
+        return GEMM_ERR_INVALID_ARG;
+    if (d.scale_mode != GEMM_SCALE_NONE && d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128)
+        return GEMM_ERR_INVALID_ARG;
+    if (d.M > INT32_MAX || d.N > INT32_MAX || d.K > INT32_MAX || d.batch > INT32_MAX)
+        return GEMM_ERR_UNSUPPORTED;
+    const bool ka = d.major_a == GEMM_K_MAJOR, kb = d.major_b == GEMM_K_MAJOR;
+    const int64_t min_lda = ka ? d.K : d.M, min_ldb = kb ? d.K : d.N;
+    if (d.lda == 0) d.lda = std::max<int64_t>(min_lda, 1);
+    if (d.ldb == 0) d.ldb = std::max<int64_t>(min_ldb, 1);
+    if (d.ldd == 0) d.ldd = std::max<int64_t>(d.N, 1);
+    if (d.lda < min_lda || d.ldb < min_ldb || d.ldd < d.N) return GEMM_ERR_INVALID_ARG;
+    const int64_t rows_a = ka ? d.M : d.K, rows_b = kb ? d.N : d.K;
+    if (d.stride_a == 0) d.stride_a = rows_a * d.lda;
+    if (d.stride_b == 0) d.stride_b = rows_b * d.ldb;
+    if (d.stride_d == 0) d.stride_d = d.M * d.ldd;
+    if (d.stride_a < 0 || d.stride_b < 0 || d.stride_d < 0) return GEMM_ERR_INVALID_ARG;
+    if (d.batch > 1 && d.stride_d < d.M * d.ldd) return GEMM_ERR_INVALID_ARG;  // outputs would overlap
+    const int64_t kblk = std::max<int64_t>(ceil_div(d.K, 128), 1);
+    if (d.ld_sa == 0) d.ld_sa = kblk;
+    if (d.ld_sb == 0) d.ld_sb = kblk;
+    if (d.stride_sa == 0) d.stride_sa = d.M * d.ld_sa;
+    if (d.stride_sb == 0) d.stride_sb = ceil_div(d.N, 128) * d.ld_sb;
+    if (d.wait_timeout_ns == 0) d.wait_timeout_ns = kDefaultTimeoutNs;
+    if (d.tile_n < 0 || d.stages < 0 || d.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+    if ((d.flags & GEMM_FLAG_CTA_GROUP_1) && (d.flags & GEMM_FLAG_CTA_GROUP_2)) return GEMM_ERR_INVALID_ARG;
+    if ((d.flags & GEMM_FLAG_SINGLE_CTA) && (d.flags & GEMM_FLAG_NO_SINGLE_CTA)) return GEMM_ERR_INVALID_ARG;
+    out->d = d;
+    return GEMM_OK;
+}
+
+bool is16(int dt) { return dt == GEMM_F16 || dt == GEMM_BF16; }
+
+gemm_status_t plan_single(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
+    const int64_t n_pad = std::max<int64_t>(round_up(d.N, 16), 16);
+    const int64_t k_pad = std::max<int64_t>(round_up(d.K, 64), 64);
+    const int64_t smem = 128 * k_pad * 2 + n_pad * k_pad * 2 + 16 + kAlignSlack;
+    if (smem > props.smem_optin_bytes) return GEMM_ERR_RESOURCES;
+    info->kernel = GEMM_KERNEL_SINGLE_CTA;
+    info->cta_group = 1;
+    info->tile_m = 128;
+    info->tile_n = (int32_t)n_pad;
+    info->tile_k = (int32_t)k_pad;
+    info->stages = 1;
+    info->tmem_stages = 1;
+    info->tmem_cols = pow2_at_least(n_pad);
+    info->grid = (int32_t)d.batch;
+    info->block_threads = 128;
+    info->num_tiles = d.batch;
+    info->stage_bytes = 128 * k_pad * 2 + n_pad * k_pad * 2;
+    info->pipeline_bytes = info->stage_bytes + 8 + 4;
+    info->smem_bytes = smem;
+    return GEMM_OK;
+}
+
+bool single_fits(const gemm_desc_t& d) {
+    return d.M <= 128 && d.N <= 256 && d.K <= 256 && is16(d.dtype_a) && d.scale_mode == GEMM_SCALE_NONE;
+}
+
+gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
+    std::memset(info, 0, sizeof(*info));
+    if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
+    if (d.dtype_d != GEMM_F32 && d.dtype_d != GEMM_BF16 && d.dtype_d != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+    if (is16(d.dtype_a)) {
+        if (d.scale_mode != GEMM_SCALE_NONE) return GEMM_ERR_UNSUPPORTED;
+    } else if (d.dtype_a == GEMM_E4M3) {
+        // block-scaled fp8 is planned by its own kernel family (not built in this version)
+        return GEMM_ERR_UNSUPPORTED;
+    } else {
+        return GEMM_ERR_UNSUPPORTED;
+    }
+    if (props.sm_count <= 0 || props.smem_optin_bytes <= 0) return GEMM_ERR_INVALID_ARG;
+
+    if (d.M == 0 || d.N == 0 || d.batch == 0 || d.K == 0) {
+        info->kernel = (d.K == 0 && d.M > 0 && d.N > 0 && d.batch > 0) ? GEMM_KERNEL_ZERO_FILL : 0;
+        info->cta_group = 1;
+        return GEMM_OK;
+    }
+
+    const bool want_single = (d.flags & GEMM_FLAG_SINGLE_CTA) != 0;
+    const bool allow_single = (d.flags & GEMM_FLAG_NO_SINGLE_CTA) == 0 &&
+                              (d.flags & (GEMM_FLAG_CTA_GROUP_1 | GEMM_FLAG_CTA_GROUP_2)) == 0 &&
+                              d.tile_n == 0 && d.stages == 0;
+    if (want_single) {
+        if (!single_fits(d)) return GEMM_ERR_UNSUPPORTED;
+        return plan_single(d, props, info);
+    }
+    if (allow_single && single_fits(d)) return plan_single(d, props, info);
+
+    // ------------------------------------------------ persistent pipeline
+    if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
+    const int out_bytes = elem_bytes(d.dtype_d);
+    const int chunk_cols = 128 / out_bytes;
+    int cg;
+    if (d.flags & GEMM_FLAG_CTA_GROUP_1) cg = 1;
+    else if (d.flags & GEMM_FLAG_CTA_GROUP_2) cg = 2;
+    else {
+        // An SM pair halves each SM's B traffic; use it when there are enough
+        // pair tiles to occupy the GPU.
+        const int64_t tn = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
+        const int64_t pair_tiles = ceil_div(d.M, 256) * ceil_div(d.N, tn) * d.batch;
+        cg = (d.M > 128 && pair_tiles >= props.sm_count / 2) ? 2 : 1;
+    }
+    int64_t tile_n = d.tile_n;
+    if (tile_n == 0) tile_n = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
+    if (tile_n % 16 != 0 || tile_n < 16 || tile_n > 256) return GEMM_ERR_UNSUPPORTED;
+    if (tile_n % chunk_cols != 0) return GEMM_ERR_UNSUPPORTED;     // epilogue writes 128-byte column chunks
+    if ((tile_n / cg) % 8 != 0) return GEMM_ERR_UNSUPPORTED;      // B half-tile rows form 8-row swizzle atoms
+    const int tmem_stages = 2;
+    const int64_t tmem_need = tmem_stages * tile_n;
+    if (tmem_need > 512) return GEMM_ERR_RESOURCES;
+    const int tmem_cols = pow2_at_least(tmem_need);
+
+    const int tile_k = 64;  // 16-bit inputs: one 128-byte swizzle row
+    const int64_t stage_a = 128 * tile_k * 2;
+    const int64_t stage_b = (tile_n / cg) * tile_k * 2;
+    const int64_t stage_bytes = stage_a + stage_b;
+    auto smem_for = [&](int64_t s) {
+        return s * stage_bytes + kStagingBytes + 8 * (2 * s + 2 * tmem_stages + 1) + 8 + kAlignSlack;
+    };
+    int64_t stages = d.stages;
+    if (stages == 0) {
+        stages = 16;
+        while (stages > 2 && smem_for(stages) > props.smem_optin_bytes) --stages;
+    }
+    if (stages < 2 || stages > 16) return GEMM_ERR_UNSUPPORTED;
+    if (smem_for(stages) > props.smem_optin_bytes) return GEMM_ERR_RESOURCES;
+
+    const int64_t num_m = ceil_div(d.M, 128 * cg);
+    const int64_t num_n = ceil_div(d.N, tile_n);
+    const int64_t tiles = num_m * num_n * d.batch;
+    if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    int64_t clusters = props.sm_count / cg;
+    if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
+    clusters = std::min<int64_t>(clusters, tiles);
+
+    info->kernel = GEMM_KERNEL_PERSISTENT;
+    info->cta_group = cg;
+    info->tile_m = 128 * cg;
+    info->tile_n = (int32_t)tile_n;
+    info->tile_k = tile_k;
+    info->stages = (int32_t)stages;
+    info->tmem_stages = tmem_stages;
+    info->tmem_cols = tmem_cols;
+    info->grid = (int32_t)(clusters * cg);
+    info->block_threads = kPersistentThreads;
+    info->num_tiles = tiles;
+    info->stage_bytes = stage_bytes;
+    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * tmem_stages) + 4;
+    info->smem_bytes = smem_for(stages);
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUtensorMapDataType tma_dtype(int dt) {
+    switch (dt) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
+}
+
+// Row-major (rows x cols) matrix, `ld` elements between rows, optional batch
+// dimension with `bstride` elements; box (box_cols x box_rows), 128-byte swizzle.
+bool encode_map(CUtensorMap* m, int dt, const void* base, int64_t cols, int64_t rows, int64_t ld, int64_t batch,
+                int64_t bstride, int box_cols, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const int eb = elem_bytes(dt);
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * eb), (cuuint64_t)(bstride * eb)};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t rank = batch > 1 ? 3 : 2;
+    CUresult r = enc(m, tma_dtype(dt), rank, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct gemm_plan_s {
+    gemm_desc_t desc;          // resolved
+    gemm_plan_info_t info;
+    gemm_device_props_t props;
+    int device;
+    gemm_device_error_t* status;  // device record
+};
+
+extern "C" {
+
+gemm_status_t gemm_plan_query(const gemm_desc_t* desc, const gemm_device_props_t* props, gemm_plan_info_t* info) {
+    if (!desc || !props || !info) return GEMM_ERR_INVALID_ARG;
+    Resolved r;
+    gemm_status_t s = resolve(desc, &r);
+    if (s != GEMM_OK) return s;
+    return plan(r.d, *props, info);
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
+    if (!out || !desc) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    Resolved r;
+    gemm_status_t s = resolve(desc, &r);
+    if (s != GEMM_OK) return s;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { g_last_cuda_error = (int)e; return GEMM_ERR_NO_DEVICE; }
+    gemm_device_props_t props{};
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+    props.sm_count = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return cuda_fail(e);
+    props.smem_optin_bytes = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return cuda_fail(e);
+    props.cc_major = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
+    props.cc_minor = v;
+    if (props.cc_major != 10 || props.cc_minor != 3) return GEMM_ERR_NO_DEVICE;  // built for sm_103a only
+    gemm_plan_info_t info;
+    s = plan(r.d, props, &info);
+    if (s != GEMM_OK) return s;
+    if (info.kernel == GEMM_KERNEL_PERSISTENT) {
+        // A persistent grid must be co-resident: cap it by the clusters the
+        // device can hold at once with this kernel's shared memory.
+        const int resident = dgb::persistent_max_active_clusters(info.cta_group, r.d.dtype_d,
+                                                                 (size_t)info.smem_bytes);
+        if (resident <= 0) return cuda_fail(cudaGetLastError());
+        if (info.grid > resident * info.cta_group) info.grid = resident * info.cta_group;
+    }
+    gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
+    if (!p) return GEMM_ERR_RESOURCES;
+    p->desc = r.d;
+    p->info = info;
+    p->props = props;
+    p->device = dev;
+    p->status = nullptr;
+    if ((e = cudaMalloc(&p->status, sizeof(gemm_device_error_t))) != cudaSuccess) {
+        delete p;
+        return cuda_fail(e);
+    }
+    if ((e = cudaMemset(p->status, 0, sizeof(gemm_device_error_t))) != cudaSuccess) {
+        cudaFree(p->status);
+        delete p;
+        return cuda_fail(e);
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info) {
+    if (!plan || !info) return GEMM_ERR_INVALID_ARG;
+    *info = plan->info;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, const float* scale_a,
+                       const float* scale_b, gemm_stream_t stream_) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const gemm_desc_t& d = plan->desc;
+    const gemm_plan_info_t& info = plan->info;
+    if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
+    if (!D) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(D)) return GEMM_ERR_ALIGNMENT;
+    const int eb_d = elem_bytes(d.dtype_d);
+    if (((d.ldd * eb_d) & 15) || ((d.batch > 1) && ((d.stride_d * eb_d) & 15))) return GEMM_ERR_ALIGNMENT;
+    const bool scaled = d.scale_mode != GEMM_SCALE_NONE;
+    if (scaled != (scale_a != nullptr) || scaled != (scale_b != nullptr)) return GEMM_ERR_INVALID_ARG;
+    cudaError_t e;
+    if (info.kernel == GEMM_KERNEL_ZERO_FILL) {
+        e = dgb::launch_zero_fill(D, d.dtype_d, d.M, d.N, d.batch, d.ldd, d.stride_d, plan->props.sm_count, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+    if (!A || !B) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B)) return GEMM_ERR_ALIGNMENT;
+    const int eb_a = elem_bytes(d.dtype_a), eb_b = elem_bytes(d.dtype_b);
+    if (((d.lda * eb_a) & 15) || ((d.ldb * eb_b) & 15)) return GEMM_ERR_ALIGNMENT;
+    if (d.batch > 1 && (((d.stride_a * eb_a) & 15) || ((d.stride_b * eb_b) & 15))) return GEMM_ERR_ALIGNMENT;
+
+    if (info.kernel == GEMM_KERNEL_SINGLE_CTA) {
+        SingleParams p{};
+        p.A = A; p.B = B; p.D = D; p.status = plan->status;
+        p.lda = d.lda; p.ldb = d.ldb; p.ldd = d.ldd;
+        p.stride_a = d.stride_a; p.stride_b = d.stride_b; p.stride_d = d.stride_d;
+        p.M = (int32_t)d.M; p.N = (int32_t)d.N; p.K = (int32_t)d.K;
+        p.n_pad = info.tile_n; p.k_pad = info.tile_k;
+        p.major_a = d.major_a; p.major_b = d.major_b;
+        p.tmem_cols = info.tmem_cols;
+        p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : 0u, 128u, (uint32_t)info.tile_n);
+        p.timeout_ns = d.wait_timeout_ns;
+        e = dgb::launch_single_cta(p, d.dtype_d, (int)d.batch, (size_t)info.smem_bytes, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+
+    // persistent pipeline
+    PersistentParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int cg = info.cta_group;
+    const int64_t batch_maps = d.batch;
+    if (!encode_map(&p.tmap_a, d.dtype_a, A, d.K, d.M, d.lda, batch_maps, d.stride_a, info.tile_k, 128) ||
+        !encode_map(&p.tmap_b, d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b, info.tile_k,
+                    info.tile_n / cg) ||
+        !encode_map(&p.tmap_d, d.dtype_d, D, d.N, d.M, d.ldd, batch_maps, d.stride_d, 128 / eb_d, 32)) {
+        g_last_cuda_error = (int)cudaErrorInvalidValue;
+        return GEMM_ERR_CUDA;
+    }
+    p.status = plan->status;
+    p.M = (int32_t)d.M; p.N = (int32_t)d.N; p.K = (int32_t)d.K; p.batch = (int32_t)d.batch;
+    p.num_m_blocks = (int32_t)ceil_div(d.M, info.tile_m);
+    p.num_n_blocks = (int32_t)ceil_div(d.N, info.tile_n);
+    p.num_k_blocks = (int32_t)ceil_div(d.K, info.tile_k);
+    p.tiles_per_batch = p.num_m_blocks * p.num_n_blocks;
+    p.num_tiles = (int32_t)info.num_tiles;
+    p.tile_n = info.tile_n;
+    p.stages = info.stages;
+    p.tmem_cols = info.tmem_cols;
+    p.tmem_stages = info.tmem_stages;
+    p.group_m = 8;
+    p.batched = d.batch > 1 ? 1 : 0;
+    p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : 0u, (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+    p.stage_bytes_a = (uint32_t)(128 * info.tile_k * eb_a);
+    p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
+    p.flags = d.flags;
+    p.timeout_ns = d.wait_timeout_ns;
+    e = dgb::launch_persistent(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, void* hD, const float* hsa,
+                            const float* hsb, void* dA, void* dB, void* dD, float* dsa, float* dsb,
+                            gemm_stream_t stream_) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const gemm_desc_t& d = plan->desc;
+    if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
+    if (!hD || !dD) return GEMM_ERR_INVALID_ARG;
+    const bool ka = d.major_a == GEMM_K_MAJOR, kb = d.major_b == GEMM_K_MAJOR;
+    // extent in elements of each operand: last element index + 1
+    const int64_t ext_a = (d.batch - 1) * d.stride_a + (ka ? (d.M - 1) * d.lda + d.K : (d.K - 1) * d.lda + d.M);
+    const int64_t ext_b = (d.batch - 1) * d.stride_b + (kb ? (d.N - 1) * d.ldb + d.K : (d.K - 1) * d.ldb + d.N);
+    const int64_t ext_d = (d.batch - 1) * d.stride_d + (d.M - 1) * d.ldd + d.N;
+    cudaError_t e;
+    if (d.K > 0) {
+        if (!hA || !hB || !dA || !dB) return GEMM_ERR_INVALID_ARG;
+        if ((e = cudaMemcpyAsync(dA, hA, (size_t)ext_a * elem_bytes(d.dtype_a), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(dB, hB, (size_t)ext_b * elem_bytes(d.dtype_b), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            return cuda_fail(e);
+        if (d.scale_mode != GEMM_SCALE_NONE) {
+            if (!hsa || !hsb || !dsa || !dsb) return GEMM_ERR_INVALID_ARG;
+            const int64_t kblk = ceil_div(d.K, 128);
+            const int64_t ext_sa = (d.batch - 1) * d.stride_sa + (d.M - 1) * d.ld_sa + kblk;
+            const int64_t ext_sb = (d.batch - 1) * d.stride_sb + (ceil_div(d.N, 128) - 1) * d.ld_sb + kblk;
+            if ((e = cudaMemcpyAsync(dsa, hsa, (size_t)ext_sa * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                return cuda_fail(e);
+            if ((e = cudaMemcpyAsync(dsb, hsb, (size_t)ext_sb * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                return cuda_fail(e);
+        }
+    }
+    gemm_status_t s = gemm_run(plan, dA, dB, dD, d.scale_mode != GEMM_SCALE_NONE ? dsa : nullptr,
+                               d.scale_mode != GEMM_SCALE_NONE ? dsb : nullptr, stream_);
+    if (s != GEMM_OK) return s;
+    if ((e = cudaMemcpyAsync(hD, dD, (size_t)ext_d * elem_bytes(d.dtype_d), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_fail(e);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream_, gemm_device_error_t* out) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    gemm_device_error_t rec;
+    cudaError_t e;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpy(&rec, plan->status, sizeof(rec), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+    if (rec.code != 0 && (e = cudaMemset(plan->status, 0, sizeof(rec))) != cudaSuccess) return cuda_fail(e);
+    if (out) *out = rec;
+    return rec.code == 0 ? GEMM_OK : (gemm_status_t)rec.code;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
+    if (!plan) return GEMM_OK;
+    cudaError_t e = cudaSuccess;
+    if (plan->status) e = cudaFree(plan->status);
+    delete plan;
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE";
+    case GEMM_ERR_RESOURCES: return "GEMM_ERR_RESOURCES";
+    default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+int gemm_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gemm_version(void) { return kVersion; }
+
+}  // extern "C"

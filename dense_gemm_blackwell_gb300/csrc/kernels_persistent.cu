@@ -1,0 +1,416 @@
+// kernels_persistent.cu -- warp-specialised persistent tcgen05 GEMM, D = A * B^T.
+//
+// Structure ("Hopper and Blackwell GEMM", concepts on warp specialisation and
+// stage count; cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", sections
+// "Depth and shared memory" and "Device side"):
+//
+//   warp 0, one lane  : TMA producer.  For every K slice of every tile it waits
+//                       for the ring slot to be empty, sets the expected bytes
+//                       on the slot's full barrier and issues two tensor copies
+//                       (A tile, B tile) that complete on it.
+//   warp 1            : allocates tensor memory (whole warp); one lane of the
+//                       pair leader issues the MMAs: waits for a full slot,
+//                       issues four K16 tcgen05.mma (the tile's first starts a
+//                       fresh accumulator), commits to the slot's empty barrier;
+//                       after the tile's last slice commits to the
+//                       accumulator's full barrier.
+//   warps 2..5        : epilogue.  Wait for a full accumulator, read it with
+//                       tcgen05.ld (one row per thread), hand the buffer back,
+//                       convert, stage 32x128 B chunks in swizzled shared
+//                       memory and write D with TMA stores (coalesced lines).
+//
+// Two accumulator buffers live in tensor memory, so the epilogue of tile t
+// overlaps the MMAs of tile t+1.  The grid is persistent: CTA (pair) c takes
+// tiles c, c+G, ... in a grouped raster that keeps a wave's A and B panels in L2.
+// Every thread follows the same tile sequence and leaves the loop together.
+//
+// cta_group::2: a cluster of two CTAs on neighbouring SMs computes a
+// (256 x tile_n) tile with one MMA stream issued by the even CTA.  Each CTA
+// loads its own 128 rows of A and its own half of B's tile_n rows into its own
+// shared memory; both CTAs' copies complete on the leader's full barrier.  The
+// leader's commits arrive on the empty / accumulator-full barriers of both
+// CTAs; each CTA's epilogue reads its own TMEM (its 128 rows) and both arrive on
+// the leader's accumulator-empty barrier.
+//
+// Every wait is bounded (wait_phase): on expiry the kernel records
+// GEMM_ERR_TIMEOUT, raises a CTA-wide abort flag, drains what it has in flight
+// (copies, MMAs, stores), frees tensor memory and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "common.cuh"
+#include "launch.h"
+
+namespace dgb {
+
+constexpr int kTileK16 = 64;               // K depth of one ring stage (16-bit inputs: 128 B)
+constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
+constexpr int kEpilogueWarps = 4;
+constexpr int kThreads = 192;
+
+__device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, int& b, int& mb, int& nb) {
+    b = t / p.tiles_per_batch;
+    const int r = t - b * p.tiles_per_batch;
+    const int span = p.group_m * p.num_n_blocks;
+    const int g = r / span;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.num_m_blocks - first_m, p.group_m);
+    const int rr = r - g * span;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+template <int CG>
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+    if constexpr (CG == 1) mma_commit(bar);
+    else mma_commit_pair(bar, 0x3);   // same barrier offset in both CTAs of the pair
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (OUT == GEMM_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <int CG, int OUT>
+__global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_constant__ PersistentParams p) {
+    constexpr int kOutBytes = (OUT == GEMM_F32) ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;   // output columns per 128-byte staging row
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int S = p.stages;
+    const int TS = p.tmem_stages;
+    const uint32_t stage_bytes = p.stage_bytes_a + p.stage_bytes_b;
+    uint8_t* ring = smem;
+    uint8_t* staging = ring + (size_t)S * stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kEpilogueWarps * 2 * kStagingBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * TS + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8u * S;
+    const uint32_t tfull0 = empty0 + 8u * S;
+    const uint32_t tempty0 = tfull0 + 8u * TS;
+    const uint32_t drain_bar = tempty0 + 8u * TS;
+    auto full = [&](int s) { return full0 + 8u * s; };
+    auto empty = [&](int s) { return empty0 + 8u * s; };
+    auto tfull = [&](int a) { return tfull0 + 8u * a; };
+    auto tempty = [&](int a) { return tempty0 + 8u * a; };
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int a = 0; a < TS; ++a) {
+            mbar_init(tfull(a), 1);
+            mbar_init(tempty(a), CG * kEpilogueWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&p.tmap_a);
+        prefetch_tensormap(&p.tmap_b);
+        prefetch_tensormap(&p.tmap_d);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int cluster_id = blockIdx.x / CG;
+    const int num_clusters = gridDim.x / CG;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool aborted = false;
+            const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
+            const int b_rows = p.tile_n / CG;
+            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+                int b, mb, nb;
+                tile_coords(p, t, b, mb, nb);
+                const int a_row = mb * (128 * CG) + (int)rank * 128;
+                const int b_row = nb * p.tile_n + (int)rank * b_rows;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase<false>(empty(stage), phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
+                                           stage, t)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t fb = (CG == 2) ? map_to_cta(full(stage), 0) : full(stage);
+                    if (leader) mbar_arrive_expect_tx(full(stage), tx_bytes);
+                    const bool drop = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0 && issued == 0;
+                    if (!drop) {
+                        const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                        const uint32_t sb = sa + p.stage_bytes_a;
+                        const int kx = kb * kTileK16;
+                        if constexpr (CG == 1) {
+                            if (p.batched) {
+                                tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
+                                tma_load_3d(sb, &p.tmap_b, fb, kx, b_row, b);
+                            } else {
+                                tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
+                                tma_load_2d(sb, &p.tmap_b, fb, kx, b_row);
+                            }
+                        } else {
+                            if (p.batched) {
+                                tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
+                                tma_load_3d_pair(sb, &p.tmap_b, fb, kx, b_row, b);
+                            } else {
+                                tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
+                                tma_load_2d_pair(sb, &p.tmap_b, fb, kx, b_row);
+                            }
+                        }
+                    }
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!aborted) {
+                // Tail: wait until the MMA released every slot, so that no commit
+                // arrives on this CTA's barriers after it exits.
+                for (int i = 0; i < S; ++i) {
+                    if (!wait_phase<false>(empty(stage), phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
+                                           stage, 0xFFFFFFFFu))
+                        break;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            } else if (leader) {
+                // Abort: wait (bounded) for the copies still in flight into the ring.
+                int s = stage;
+                uint32_t ph = phase;
+                const int n = issued < S ? issued : S;
+                for (int i = 0; i < n; ++i) {
+                    if (s == 0) { s = S - 1; ph ^= 1u; } else { --s; }
+                    wait_phase_drain(full(s), ph, tmo);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool aborted = false;
+            bool issued_any = false;
+            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+                if (!wait_phase<CG == 2>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma,
+                                         acc, t)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                    const uint64_t da = smem_desc_sw128(sa);
+                    const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
+#pragma unroll
+                    for (int kk = 0; kk < kTileK16 / 16; ++kk)
+                        mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb | kk) != 0);
+                    issued_any = true;
+                    commit_to<CG>(empty(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (aborted) break;
+                commit_to<CG>(tfull(acc));
+                if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (aborted && issued_any) {
+                // Abort: make sure every MMA issued so far has finished before TMEM is freed.
+                if constexpr (CG == 1) mma_commit(drain_bar);
+                else mma_commit_pair(drain_bar, 0x1);
+                wait_phase_drain(drain_bar, 0, tmo);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp & 3;                 // TMEM lanes [32*wq, 32*wq+32) are this warp's
+        uint8_t* my_staging = staging + (warp - 2) * 2 * kStagingBytes;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int chunk_no = 0;
+        const int nchunks = p.tile_n / kChunkCols;
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            int b, mb, nb;
+            tile_coords(p, t, b, mb, nb);
+            int ok = 0;
+            if (lane == 0)
+                ok = wait_phase<false>(tfull(acc), acc_phase, abort_flag, tmo, p.status, kRoleEpilogue, acc, t);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
+            const int m0 = mb * (128 * CG) + (int)rank * 128 + wq * 32;
+            const int n0 = nb * p.tile_n;
+            for (int c = 0; c < nchunks; ++c) {
+                uint32_t w[32];
+                if constexpr (OUT == GEMM_F32) {
+                    tmem_ld_32x32b_x32(t_lane + c * 32, w);
+                    tmem_wait_ld();
+                    tmem_reg_fence(w);
+                } else {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(t_lane + c * 64, r0);
+                    tmem_ld_32x32b_x32(t_lane + c * 64 + 32, r1);
+                    tmem_wait_ld();
+                    tmem_reg_fence(r0);
+                    tmem_reg_fence(r1);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        w[i] = pack2<OUT>(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                        w[16 + i] = pack2<OUT>(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+                    }
+                }
+                if (c == nchunks - 1) {
+                    // Every TMEM read of this tile is complete: hand the buffer back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1) mbar_arrive(tempty(acc));
+                        else mbar_arrive_remote(map_to_cta(tempty(acc), 0));
+                    }
+                }
+                // The staging buffer used two chunks ago must have been read by its store.
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t* buf = my_staging + (chunk_no & 1) * kStagingBytes;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int x = n0 + c * kChunkCols;
+                if (lane == 0 && m0 < p.M && x < p.N) {
+                    if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
+                    else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                    bulk_commit_group();
+                }
+                ++chunk_no;
+            }
+            if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+template <int CG, int OUT>
+static cudaError_t launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
+    auto kern = persistent_kernel<CG, OUT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int CG, int OUT>
+static int max_clusters_typed(size_t smem) {
+    auto kern = persistent_kernel<CG, OUT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CG, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+int persistent_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes) {
+    if (cta_group == 1) {
+        switch (dtype_d) {
+        case GEMM_F32: return max_clusters_typed<1, GEMM_F32>(smem_bytes);
+        case GEMM_BF16: return max_clusters_typed<1, GEMM_BF16>(smem_bytes);
+        case GEMM_F16: return max_clusters_typed<1, GEMM_F16>(smem_bytes);
+        default: return 0;
+        }
+    }
+    switch (dtype_d) {
+    case GEMM_F32: return max_clusters_typed<2, GEMM_F32>(smem_bytes);
+    case GEMM_BF16: return max_clusters_typed<2, GEMM_BF16>(smem_bytes);
+    case GEMM_F16: return max_clusters_typed<2, GEMM_F16>(smem_bytes);
+    default: return 0;
+    }
+}
+
+cudaError_t launch_persistent(const PersistentParams& p, int cta_group, int dtype_d, int grid,
+                              size_t smem_bytes, cudaStream_t stream) {
+    if (cta_group == 1) {
+        switch (dtype_d) {
+        case GEMM_F32: return launch_typed<1, GEMM_F32>(p, grid, smem_bytes, stream);
+        case GEMM_BF16: return launch_typed<1, GEMM_BF16>(p, grid, smem_bytes, stream);
+        case GEMM_F16: return launch_typed<1, GEMM_F16>(p, grid, smem_bytes, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (dtype_d) {
+    case GEMM_F32: return launch_typed<2, GEMM_F32>(p, grid, smem_bytes, stream);
+    case GEMM_BF16: return launch_typed<2, GEMM_BF16>(p, grid, smem_bytes, stream);
+    case GEMM_F16: return launch_typed<2, GEMM_F16>(p, grid, smem_bytes, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dgb

@@ -1,0 +1,213 @@
+/*
+ * gemm.h -- C ABI of a dense GEMM for one NVIDIA GB300 (sm_103a).
+ *
+ * Computes, for every batch entry b:
+ *
+ *     D[b] = A[b] * B[b]^T          (fp32 accumulation, one rounding to D's type)
+ *
+ * "Out = A @ B.T" is the product of the TVM TIRx "Blackwell Tensor Cores"
+ * guide (section "The Accumulator's Lifetime"); accumulation starts fresh on
+ * the first K slice and there is no alpha/beta -- scaling belongs to the
+ * caller (TVM TIRx "mma.sync", section "Accumulation, transpose and
+ * alpha/beta").  Block-scaled 8-bit inputs multiply every 1x128 block of a
+ * row of A and every 128x128 block of B by its own fp32 scale ("Hopper and
+ * Blackwell GEMM", concept "FP8 and FP4, with block scaling").
+ *
+ * Element addressing (elements, not bytes):
+ *   A, K-major  : A[b*stride_a + m*lda + k]    A, MN-major : A[b*stride_a + k*lda + m]
+ *   B, K-major  : B[b*stride_b + n*ldb + k]    B, MN-major : B[b*stride_b + k*ldb + n]
+ *   D (row-major): D[b*stride_d + m*ldd + n]
+ *   scale_a     : scale_a[b*stride_sa + m*ld_sa + k/128]           (block-scaled only)
+ *   scale_b     : scale_b[b*stride_sb + (n/128)*ld_sb + k/128]     (block-scaled only)
+ * "row-major A, column-major B" in BLAS terms is K-major A and K-major B (TN).
+ *
+ * Ownership: the caller owns every device buffer and the stream; the library
+ * never frees or retains them past the call that uses them.  A plan owns its
+ * host state and one small device status record (allocated by
+ * gemm_plan_create, freed by gemm_plan_destroy).
+ *
+ * Errors: every call returns a gemm_status_t; nothing throws across the ABI.
+ * Unsupported combinations fail with GEMM_ERR_UNSUPPORTED -- never a silent
+ * fallback to another kernel or to the CPU.
+ *
+ * Threading: calls on different plans are independent.  One plan may be run
+ * on one stream at a time (its status record is shared by its launches).
+ */
+#ifndef DENSE_GEMM_BLACKWELL_GB300_GEMM_H
+#define DENSE_GEMM_BLACKWELL_GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, bad leading dim */
+    GEMM_ERR_UNSUPPORTED = 2,  /* valid request this library does not implement */
+    GEMM_ERR_ALIGNMENT = 3,    /* pointer or stride not a multiple of 16 bytes */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (see gemm_last_cuda_error) */
+    GEMM_ERR_TIMEOUT = 5,      /* a device-side wait ran out; reported by gemm_sync_status */
+    GEMM_ERR_NO_DEVICE = 6,    /* no sm_103 device is current */
+    GEMM_ERR_RESOURCES = 7     /* shared/tensor memory budget cannot hold the requested tile */
+} gemm_status_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_F32 = 3 } gemm_dtype_t;
+typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
+typedef enum { GEMM_SCALE_NONE = 0, GEMM_SCALE_BLOCK_1x128_128x128 = 1 } gemm_scale_mode_t;
+
+/* Kernel families a plan can select. */
+typedef enum {
+    GEMM_KERNEL_SINGLE_CTA = 1,   /* one CTA per problem, threads stage operands (small problems) */
+    GEMM_KERNEL_PERSISTENT = 2,   /* warp-specialised persistent TMA/tcgen05 pipeline */
+    GEMM_KERNEL_FP8_BLOCK = 3,    /* persistent pipeline with per-block scale promotion */
+    GEMM_KERNEL_ZERO_FILL = 4     /* K == 0: D is written with zeros */
+} gemm_kernel_t;
+
+/* gemm_desc_t.flags */
+#define GEMM_FLAG_CTA_GROUP_1     (1u << 0)  /* force the single-SM MMA form */
+#define GEMM_FLAG_CTA_GROUP_2     (1u << 1)  /* force the SM-pair (cta_group::2) MMA form */
+#define GEMM_FLAG_NO_SINGLE_CTA   (1u << 2)  /* never choose GEMM_KERNEL_SINGLE_CTA */
+#define GEMM_FLAG_SINGLE_CTA      (1u << 3)  /* require GEMM_KERNEL_SINGLE_CTA */
+#define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
+                                                the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
+
+/* One GEMM problem.  Zero-valued optional fields take the documented default. */
+typedef struct {
+    int64_t M, N, K;        /* D is M x N per batch entry; K is the contraction length */
+    int64_t batch;          /* number of independent problems (>= 1; 0 = no-op) */
+    int32_t dtype_a, dtype_b;   /* gemm_dtype_t: F16+F16, BF16+BF16, or E4M3+E4M3 (block-scaled) */
+    int32_t dtype_d;            /* gemm_dtype_t: F32, BF16 or F16 */
+    int32_t major_a, major_b;   /* gemm_major_t */
+    int32_t scale_mode;         /* gemm_scale_mode_t; BLOCK requires E4M3 inputs */
+    int64_t lda, ldb, ldd;      /* leading dims in elements; 0 = packed (K or M/N, and N for D) */
+    int64_t stride_a, stride_b, stride_d;  /* elements between batch entries; 0 = packed */
+    int64_t ld_sa, ld_sb;       /* scale leading dims in floats; 0 = ceil(K/128) */
+    int64_t stride_sa, stride_sb;  /* floats between batch entries of the scales; 0 = packed */
+    uint32_t flags;             /* GEMM_FLAG_* */
+    int32_t tile_n;             /* N extent of one MMA tile (multiple of 16, 16..256); 0 = planner */
+    int32_t stages;             /* shared-memory ring depth (2..16); 0 = planner */
+    int32_t max_ctas;           /* cap on persistent CTAs; 0 = all SMs */
+    uint64_t wait_timeout_ns;   /* bound on every device-side wait; 0 = 2 s */
+} gemm_desc_t;
+
+/* The planner's decisions, as gemm_plan_query / gemm_plan_info report them. */
+typedef struct {
+    int32_t kernel;          /* gemm_kernel_t */
+    int32_t cta_group;       /* 1 or 2 SMs per MMA */
+    int32_t tile_m;          /* M extent of one MMA tile (128 per SM) */
+    int32_t tile_n;          /* N extent of one MMA tile */
+    int32_t tile_k;          /* K depth of one ring stage (64 for 16-bit, 128 for 8-bit inputs) */
+    int32_t stages;          /* shared-memory ring depth */
+    int32_t tmem_stages;     /* accumulator buffers in tensor memory */
+    int32_t tmem_cols;       /* tensor-memory columns allocated per CTA (power of two, <= 512) */
+    int32_t grid;            /* CTAs launched */
+    int32_t block_threads;   /* threads per CTA */
+    int64_t num_tiles;       /* output tiles over all batch entries */
+    int64_t stage_bytes;     /* bytes of one ring stage per CTA */
+    int64_t pipeline_bytes;  /* ring + 8 B per barrier (2 per stage, 2 per TMEM stage) + 4 B TMEM handle */
+    int64_t smem_bytes;      /* dynamic shared memory per CTA, all included */
+} gemm_plan_info_t;
+
+/* Device properties the planner depends on (gemm_plan_query takes them explicitly). */
+typedef struct {
+    int32_t sm_count;            /* streaming multiprocessors */
+    int32_t smem_optin_bytes;    /* cudaDevAttrMaxSharedMemoryPerBlockOptin */
+    int32_t cc_major, cc_minor;  /* compute capability; this library runs on 10.3 only */
+} gemm_device_props_t;
+
+/* Device-side error record (gemm_sync_status). */
+typedef struct {
+    uint32_t code;    /* GEMM_OK or GEMM_ERR_TIMEOUT */
+    uint32_t role;    /* 1 = TMA producer, 2 = MMA issuer, 3 = epilogue, 4 = single-CTA kernel */
+    uint32_t stage;   /* ring stage or accumulator buffer being waited on */
+    uint32_t tile;    /* linear output tile index */
+    uint32_t block;   /* blockIdx.x of the CTA that timed out */
+    uint32_t reserved[3];
+} gemm_device_error_t;
+
+typedef struct gemm_plan_s* gemm_plan_t;
+
+/*
+ * gemm_plan_query -- plan a problem for the given device properties without
+ * touching any GPU (host arithmetic only).  Checks the descriptor's gates --
+ * supported element types, tile shape legality (tcgen05: N a multiple of 16
+ * up to 256, the accumulator within 512 tensor-memory columns), ring depth
+ * within the shared-memory budget -- and fills *info.  The budget arithmetic
+ * follows the cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", section
+ * "Depth and shared memory": one stage holds an A and a B tile, plus 8 bytes
+ * per barrier and a 4-byte tensor-memory handle.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED or GEMM_ERR_RESOURCES.
+ */
+gemm_status_t gemm_plan_query(const gemm_desc_t* desc, const gemm_device_props_t* props,
+                              gemm_plan_info_t* info);
+
+/*
+ * gemm_plan_create -- plan a problem on the current CUDA device and allocate
+ * the plan's device status record.  *plan receives an opaque handle.
+ * Returns GEMM_OK, or the gemm_plan_query codes, GEMM_ERR_NO_DEVICE (current
+ * device is not compute capability 10.3) or GEMM_ERR_CUDA.
+ */
+gemm_status_t gemm_plan_create(gemm_plan_t* plan, const gemm_desc_t* desc);
+
+/* gemm_plan_info -- copy the plan's decisions into *info. */
+gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info);
+
+/*
+ * gemm_run -- enqueue D = A * B^T on `stream` (asynchronous, stream-ordered).
+ * A, B, D are device pointers laid out as described at the top of this file;
+ * scale_a / scale_b are device pointers for GEMM_SCALE_BLOCK_1x128_128x128 and
+ * must be NULL otherwise.  A, B, D (and scales) must be 16-byte aligned and
+ * every leading dimension / batch stride a multiple of 16 bytes
+ * (GEMM_ERR_ALIGNMENT).  M, N or batch equal to 0 is a no-op; K equal to 0
+ * writes zeros to D.  Tensor maps are encoded per call from the pointers.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT or GEMM_ERR_CUDA.
+ * Device-side wait expiry is not visible here; see gemm_sync_status.
+ */
+gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
+                       const float* scale_a, const float* scale_b, gemm_stream_t stream);
+
+/*
+ * gemm_run_host -- the same product for operands that live in host memory.
+ * Copies hA, hB (and the scales) into the caller's device buffers dA, dB
+ * (dsa, dsb), runs gemm_run into dD and copies dD back into hD, all enqueued
+ * on `stream` with cudaMemcpyAsync (pinned host memory makes the copies
+ * asynchronous).  Host and device buffers share the plan's layout (leading
+ * dims and batch strides) and each must span that layout's extent.  The call
+ * returns once the work is enqueued; synchronise `stream` before reading hD.
+ */
+gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, void* hD,
+                            const float* hscale_a, const float* hscale_b,
+                            void* dA, void* dB, void* dD, float* dscale_a, float* dscale_b,
+                            gemm_stream_t stream);
+
+/*
+ * gemm_sync_status -- synchronise `stream`, read the plan's device error
+ * record into *out (may be NULL), reset it, and return its code: GEMM_OK, or
+ * GEMM_ERR_TIMEOUT when a bounded device-side wait ran out in a launch since
+ * the last call (the kernel then released its resources and returned).
+ */
+gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream, gemm_device_error_t* out);
+
+/* gemm_plan_destroy -- free the plan and its status record (NULL is allowed). */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* gemm_status_string -- static, human-readable name of a status code. */
+const char* gemm_status_string(gemm_status_t status);
+
+/* gemm_last_cuda_error -- the cudaError_t of the most recent GEMM_ERR_CUDA on this thread. */
+int gemm_last_cuda_error(void);
+
+/* gemm_version -- library version, major*10000 + minor*100 + patch. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_BLACKWELL_GB300_GEMM_H */
