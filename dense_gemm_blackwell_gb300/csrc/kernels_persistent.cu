@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         uint8_t* my_staging = staging + (warp - 2) * 2 * kStagingBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int chunk_no = 0;
+        int stores = 0;                          // TMA stores issued; selects the staging buffer
         const int nchunks = p.tile_n / kChunkCols;
         for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
             int b, mb, nb;
@@ -277,7 +277,20 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
             const int m0 = mb * (128 * CG) + (int)rank * 128 + wq * 32;
             const int n0 = nb * p.tile_n;
-            for (int c = 0; c < nchunks; ++c) {
+            // Chunks that hold at least one in-range column of an in-range row; the
+            // rest of the tile (padding beyond M or N) is neither read nor stored.
+            const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
+            auto release = [&]() {
+                // Every TMEM read of this tile by this warp is complete: hand the buffer back.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 1) mbar_arrive(tempty(acc));
+                    else mbar_arrive_remote(map_to_cta(tempty(acc), 0));
+                }
+            };
+            if (n_valid == 0) release();
+            for (int c = 0; c < n_valid; ++c) {
                 uint32_t w[32];
                 if constexpr (OUT == GEMM_F32) {
                     tmem_ld_32x32b_x32(t_lane + c * 32, w);
@@ -296,32 +309,24 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                         w[16 + i] = pack2<OUT>(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
                     }
                 }
-                if (c == nchunks - 1) {
-                    // Every TMEM read of this tile is complete: hand the buffer back.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 1) mbar_arrive(tempty(acc));
-                        else mbar_arrive_remote(map_to_cta(tempty(acc), 0));
-                    }
-                }
-                // The staging buffer used two chunks ago must have been read by its store.
+                if (c == n_valid - 1) release();
+                // The staging buffer written two stores ago must have been read by that store.
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
-                uint8_t* buf = my_staging + (chunk_no & 1) * kStagingBytes;
+                uint8_t* buf = my_staging + (stores & 1) * kStagingBytes;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                         make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int x = n0 + c * kChunkCols;
-                if (lane == 0 && m0 < p.M && x < p.N) {
+                if (lane == 0) {
+                    const int x = n0 + c * kChunkCols;
                     if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
                     else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
                     bulk_commit_group();
                 }
-                ++chunk_no;
+                ++stores;
             }
             if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
         }

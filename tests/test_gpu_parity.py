@@ -81,7 +81,7 @@ def test_single_cta_example_uniform():
 
 @pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
 def test_single_cta_ragged_batched(out):
-    prob = inputs.make("single_cta", M=100, N=40, K=100, batch=3, seed=9)
+    prob = inputs.make("single_cta", M=100, N=40, K=104, batch=3, seed=9)   # rows of 208 B: 16-B multiples
     prob.wl.dtype_in = "bf16"
     prob.A, prob.B = prob.A.float().bfloat16(), prob.B.float().bfloat16()
     check_full(prob, out)
@@ -89,7 +89,7 @@ def test_single_cta_ragged_batched(out):
 
 def test_single_cta_mn_major():
     g = torch.Generator().manual_seed(10)
-    M, N, K = 77, 56, 90
+    M, N, K = 80, 56, 90   # MN-major rows are M (resp. N) long: 160 B and 112 B
     a = torch.randint(-3, 4, (M, K), generator=g).half()
     b = torch.randint(-3, 4, (N, K), generator=g).half()
     at, bt = a.t().contiguous().cuda(), b.t().contiguous().cuda()     # [K][M], [K][N]
@@ -107,7 +107,7 @@ def test_single_cta_mn_major():
 
 @pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
 def test_persistent_integers_bit_exact(cg_flag):
-    prob = inputs.make("square8192_bf16", M=520, N=600, K=333, dist="ints", seed=11)
+    prob = inputs.make("square8192_bf16", M=520, N=600, K=336, dist="ints", seed=11)   # K tail of 16
     r, info = check_full(prob, "f32", exact=True, flags=cg_flag)
     assert info["kernel"] == dg.GEMM_KERNEL_PERSISTENT
     assert info["cta_group"] == (1 if cg_flag == dg.GEMM_FLAG_CTA_GROUP_1 else 2)
