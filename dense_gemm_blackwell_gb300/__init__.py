@@ -17,7 +17,7 @@ from ._build import LIB as _LIB_PATH, build as _build
 
 __all__ = [
     "build", "lib", "GemmError", "GemmDesc", "GemmPlanInfo", "GemmDeviceProps", "GemmDeviceError",
-    "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host",
+    "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host", "gemm_run_noalloc",
     "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
     "gemm_version", "Plan", "matmul", "header_functions",
 ]
@@ -115,6 +115,9 @@ def lib():
                 L.gemm_run.restype = st
                 L.gemm_run_host.argtypes = [vp] * 12
                 L.gemm_run_host.restype = st
+                L.gemm_run_noalloc.argtypes = [ctypes.POINTER(GemmDesc), vp, vp, vp, vp, vp, vp,
+                                               ctypes.POINTER(GemmDeviceError)]
+                L.gemm_run_noalloc.restype = st
                 L.gemm_sync_status.argtypes = [vp, vp, ctypes.POINTER(GemmDeviceError)]
                 L.gemm_sync_status.restype = st
                 L.gemm_plan_destroy.argtypes = [vp]
@@ -163,6 +166,12 @@ def gemm_run(plan, A, B, D, scale_a=None, scale_b=None, stream=None) -> int:
 
 def gemm_run_host(plan, hA, hB, hD, hsa, hsb, dA, dB, dD, dsa, dsb, stream=None) -> int:
     return lib().gemm_run_host(plan, hA, hB, hD, hsa, hsb, dA, dB, dD, dsa, dsb, stream)
+
+
+def gemm_run_noalloc(desc: GemmDesc, A, B, D, scale_a=None, scale_b=None, stream=None, status_out=None) -> int:
+    """Allocation-free product (see include/gemm.h); status_out: a GemmDeviceError or None."""
+    ref = ctypes.byref(status_out) if status_out is not None else None
+    return lib().gemm_run_noalloc(ctypes.byref(desc), A, B, D, scale_a, scale_b, stream, ref)
 
 
 def gemm_sync_status(plan, stream=None):

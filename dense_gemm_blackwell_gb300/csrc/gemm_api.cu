@@ -281,6 +281,44 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+// ---------------------------------------------------------------- allocation-free variant state
+//
+// gemm_run_noalloc keeps the kernels' device error record in this array
+// instead of a cudaMalloc'd one.  It is library-owned device memory: every GPU
+// that loads the library holds these bytes until the process exits.  Host code
+// must not pass the name itself to a kernel (on the host it is only a stand-in);
+// its device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[256];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Zero the first `bytes` of the record in stream order (names the array directly).
+__global__ void noalloc_clear_kernel(unsigned bytes) {
+    for (unsigned i = threadIdx.x; i < bytes && i < sizeof(g_noalloc_scratch); i += blockDim.x)
+        g_noalloc_scratch[i] = 0;
+}
+
+// Device address of g_noalloc_scratch on device `dev` (current), looked up on
+// the first call for that device.
+gemm_status_t noalloc_address(int dev, void** out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
 struct gemm_plan_s {
     gemm_desc_t desc;          // resolved
     gemm_plan_info_t info;
@@ -478,6 +516,54 @@ gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream_, gemm_dev
     if (rec.code != 0 && (e = cudaMemset(plan->status, 0, sizeof(rec))) != cudaSuccess) return cuda_fail(e);
     if (out) *out = rec;
     return rec.code == 0 ? GEMM_OK : (gemm_status_t)rec.code;
+}
+
+gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, void* D,
+                               const float* scale_a, const float* scale_b, gemm_stream_t stream_,
+                               gemm_device_error_t* status_out) {
+    if (!desc) return GEMM_ERR_INVALID_ARG;
+    Resolved r;
+    gemm_status_t s = resolve(desc, &r);
+    if (s != GEMM_OK) return s;
+    // The only device memory the kernels use beyond A, B, D and the scales is
+    // their error record; it must fit the static array.
+    if (sizeof(gemm_device_error_t) > sizeof(g_noalloc_scratch)) return GEMM_ERR_RESOURCES;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { g_last_cuda_error = (int)e; return GEMM_ERR_NO_DEVICE; }
+    gemm_plan_s p{};
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+    p.props.sm_count = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return cuda_fail(e);
+    p.props.smem_optin_bytes = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return cuda_fail(e);
+    p.props.cc_major = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
+    p.props.cc_minor = v;
+    if (p.props.cc_major != 10 || p.props.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    s = plan(r.d, p.props, &p.info);
+    if (s != GEMM_OK) return s;
+    if (p.info.kernel == GEMM_KERNEL_PERSISTENT) {
+        const int resident = dgb::persistent_max_active_clusters(p.info.cta_group, r.d.dtype_d,
+                                                                 (size_t)p.info.smem_bytes);
+        if (resident <= 0) return cuda_fail(cudaGetLastError());
+        if (p.info.grid > resident * p.info.cta_group) p.info.grid = resident * p.info.cta_group;
+    }
+    void* record = nullptr;
+    if ((s = noalloc_address(dev, &record)) != GEMM_OK) return s;
+    p.desc = r.d;
+    p.device = dev;
+    p.status = static_cast<gemm_device_error_t*>(record);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    noalloc_clear_kernel<<<1, 32, 0, stream>>>((unsigned)sizeof(gemm_device_error_t));
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    s = gemm_run(&p, A, B, D, scale_a, scale_b, stream_);
+    if (s != GEMM_OK || status_out == nullptr) return s;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpy(status_out, record, sizeof(*status_out), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    return status_out->code == 0 ? GEMM_OK : (gemm_status_t)status_out->code;
 }
 
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {

@@ -194,6 +194,37 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, vo
  */
 gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream, gemm_device_error_t* out);
 
+/*
+ * gemm_run_noalloc -- D = A * B^T without any device allocation.  The pages
+ * have no counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc, which gemm_plan_create does for its error record: code whose
+ * device memory is entirely owned by a framework's caching pool (an allocation
+ * behind the pool's back can fail for lack of memory or fragment it), and
+ * latency-critical loops that cannot afford the device-wide synchronisation a
+ * cudaMalloc or cudaFree may imply.
+ *
+ * Arguments are those of gemm_plan_create followed by those of gemm_run; the
+ * problem is planned on the current device on every call (host arithmetic and
+ * device-attribute queries, nothing allocated).  The kernels' device error
+ * record lives in a library-owned static device array of 256 bytes (the
+ * record needs 32), which every GPU that loads the library holds until the
+ * process exits; no problem size needs more, and a build whose record did not
+ * fit would return GEMM_ERR_RESOURCES.  The first call on each device looks up
+ * the array's device address; make that first call before any stream capture.
+ * Each call clears the record on `stream`, then enqueues the product; the
+ * record keeps the last call's contents.  All calls share this one record, so
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it.
+ *
+ * status_out: NULL returns once the work is enqueued; otherwise the call
+ * synchronises `stream`, copies the record into *status_out and returns its
+ * code (GEMM_OK or GEMM_ERR_TIMEOUT).  Other returns: the codes of
+ * gemm_plan_create and gemm_run.
+ */
+gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, void* D,
+                               const float* scale_a, const float* scale_b, gemm_stream_t stream,
+                               gemm_device_error_t* status_out);
+
 /* gemm_plan_destroy -- free the plan and its status record (NULL is allowed). */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
