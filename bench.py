@@ -54,6 +54,14 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured HBM copy (MEASURED_PEAKS.json)"
+    except Exception:
+        return 6800.0, "fallback 6.8 TB/s"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -138,62 +146,117 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
-def cpu_oracle_sample(seconds_target: float, prob=None):
+def _oracle_rows(prob, rows, ncols=None):
+    """The oracle on selected rows (and optionally the first ncols columns)."""
+    import oracle
+    wl = prob.wl
+    N = wl.N if ncols is None else ncols
+    B = prob.B if ncols is None else (prob.B[..., :N, :] if wl.batch == 1 else prob.B[:, :N, :]).contiguous()
+    kw = dict(M=wl.M, N=N, K=wl.K, batch=wl.batch, dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
+    if wl.block_scaled:
+        sb = prob.scale_b.numpy()[: (N + 127) // 128]
+        kw.update(scale_a=prob.scale_a.numpy(), scale_b=sb, ld_sb=prob.scale_b.shape[1])
+    oracle.gemm_rows(prob.A, B, rows=rows, **kw)
+
+
+def cpu_oracle_sample(seconds_target: float, prob=None, unit=UNIT):
     """Time the CPU oracle on a bounded row sample of the workload.  Returns
-    (tflops, cores, sample description, seconds)."""
+    (value in `unit`, cores, sample description, seconds)."""
     import oracle
     from dense_gemm_blackwell_gb300 import inputs
     if prob is None:
         prob = inputs.make(WORKLOAD)
     wl = prob.wl
-    kw = dict(M=wl.M, N=wl.N, K=wl.K, dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
     t = time.perf_counter()
-    oracle.gemm_rows(prob.A, prob.B, rows=list(range(2)), **kw)
-    per_row = max((time.perf_counter() - t) / 2, 1e-4)
-    rows = max(2, min(wl.M, int(seconds_target / per_row)))
+    _oracle_rows(prob, list(range(2)))
+    per_row = max((time.perf_counter() - t) / 2, 1e-5)
+    rows = max(2, min(wl.M * wl.batch, int(seconds_target / per_row)))
     t = time.perf_counter()
-    oracle.gemm_rows(prob.A, prob.B, rows=list(range(rows)), **kw)
+    _oracle_rows(prob, list(range(rows)))
     dt = time.perf_counter() - t
     flops = 2.0 * rows * wl.N * wl.K
-    desc = "%d of %d rows of D (all %d columns, K=%d) of %s, fp64 oracle" % (rows, wl.M, wl.N, wl.K, wl.name)
+    desc = "%d of %d rows of D (all %d columns, K=%d) of %s, fp64 oracle" % (rows, wl.M * wl.batch, wl.N, wl.K, wl.name)
+    if unit == "GB/s":
+        frac = rows / float(wl.M * wl.batch)
+        total = sum(t_.numel() * t_.element_size() for t_ in (prob.A, prob.B)) + wl.M * wl.N * wl.batch * 2
+        return total * frac / dt / 1e9, oracle.num_threads(), desc, dt
+    if unit == "us/launch":
+        return dt * 1e6 * (wl.M * wl.batch) / rows, oracle.num_threads(), desc, dt
     return flops / dt / 1e12, oracle.num_threads(), desc, dt
 
 
 def run_reference(args):
+    """The CPU oracle, as it stands, on this host's cores: each step is a bounded
+    sample (rows, and if one row is too long for the budget, leading columns)
+    of the workload; rank 0 only."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     from dense_gemm_blackwell_gb300 import inputs
-    prob = inputs.make(WORKLOAD)
+    winfo = WORKLOAD_INFO[args.workload]
+    prob = inputs.make(args.workload)
     wl = prob.wl
-    kw = dict(M=wl.M, N=wl.N, K=wl.K, dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
     t = time.perf_counter()
-    oracle.gemm_rows(prob.A, prob.B, rows=[0, 1], **kw)
-    per_row = max((time.perf_counter() - t) / 2, 1e-4)
-    budget = 150.0  # seconds for warmup + timed steps together
-    rows = max(1, int(budget / max(args.steps + args.warmup, 1) / per_row))
-    rows = min(rows, wl.M)
-    for i in range(args.warmup):
-        oracle.gemm_rows(prob.A, prob.B, rows=list(range(rows)), **kw)
+    _oracle_rows(prob, [0, 1])
+    per_row = max((time.perf_counter() - t) / 2, 1e-5)
+    budget = 150.0  # seconds for warm-up + timed steps together
+    per_step = budget / max(args.steps + args.warmup, 1)
+    rows = max(1, min(wl.M * wl.batch, int(per_step / per_row)))
+    ncols = wl.N
+    if per_row > per_step:
+        ncols = max(16, min(wl.N, int(wl.N * per_step / per_row)))
+    sample_rows = list(range(rows))
+    for _ in range(args.warmup):
+        _oracle_rows(prob, sample_rows, ncols)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        oracle.gemm_rows(prob.A, prob.B, rows=list(range(rows)), **kw)
+    for _ in range(args.steps):
+        _oracle_rows(prob, sample_rows, ncols)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * wl.N * wl.K * args.steps
-    value = flops / dt / 1e12
-    sample = "each step: %d of %d rows of D (all %d columns, K=%d), fp64 oracle" % (rows, wl.M, wl.N, wl.K)
+    frac = rows * ncols / float(wl.M * wl.batch * wl.N)
+    work_s = dt / max(args.steps, 1) / frac          # seconds for the whole product at this rate
+    if winfo["unit"] == "GB/s":
+        total = sum(t_.numel() * t_.element_size() for t_ in (prob.A, prob.B)) + wl.M * wl.N * wl.batch * 2
+        value = total / work_s / 1e9
+    elif winfo["unit"] == "us/launch":
+        value = work_s * 1e6
+    else:
+        value = wl.flops / work_s / 1e12
+    sample = "each step: %d of %d rows x %d of %d columns of D (K=%d), fp64 oracle" % (
+        rows, wl.M * wl.batch, ncols, wl.N, wl.K)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(args.steps, 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": wl.M, "N": wl.N, "K": wl.K, "inputs": "bf16 U[-1,1] seed %d" % wl.seed},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+        "impl": "reference", "metric": winfo["metric"], "value": value, "unit": winfo["unit"],
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(args.steps, 1),
+        "higher_is_better": winfo["unit"] != "us/launch", "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: %s" % (args.workload, winfo["text"]), "M": wl.M, "N": wl.N, "K": wl.K,
+                   "batch": wl.batch, "inputs": "%s seed %d" % (wl.dist, wl.seed)},
+        "cpu_baseline": {"value": value, "unit": winfo["unit"], "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": winfo["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# Per-workload metric and roofline bound.  The default workload is the headline.
+WORKLOAD_INFO = {
+    "square8192_bf16": dict(metric=METRIC, unit=UNIT, bound="tensor", peak_ratio=1.0,
+                            text="D = A*B^T, M=N=K=8192, bf16 TN, fp32 accumulate, fp32 out"),
+    "square4096_bf16": dict(metric="GEMM TFLOP/s (bf16 in, fp32 acc, bf16 out, 4096^3)", unit=UNIT,
+                            bound="tensor", peak_ratio=1.0,
+                            text="D = A*B^T, M=N=K=4096, bf16 TN, fp32 accumulate, bf16 out"),
+    "batched256_f16": dict(metric="batched GEMM GB/s (512 x 256^3, f16 in/out, fp32 acc)", unit="GB/s",
+                           bound="hbm", peak_ratio=1.0,
+                           text="512 independent D = A*B^T of 256^3, f16 TN, fp32 accumulate, f16 out"),
+    "fp8_block8192": dict(metric="GEMM TFLOP/s (e4m3 block-scaled in, fp32 acc, bf16 out, 8192^3)", unit=UNIT,
+                          bound="tensor", peak_ratio=2.0,
+                          text="D = (qA sA)(qB sB)^T, 8192^3, e4m3 TN, fp32 scales 1x128 / 128x128, bf16 out"),
+    "single_cta": dict(metric="single-CTA GEMM latency (128x64x64 f16 -> f32)", unit="us/launch",
+                       bound="latency", peak_ratio=1.0,
+                       text="Out = A @ B.T, A 128x64, B 64x64 f16, fp32 out, one CTA"),
+}
 
 
 def run_ours(args):
@@ -208,21 +271,31 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
-    prob = inputs.make(WORKLOAD)
+    winfo = WORKLOAD_INFO[args.workload]
+    prob = inputs.make(args.workload)
     wl = prob.wl
     dg.build()
+    code = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32, "e4m3": dg.GEMM_E4M3}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     A = prob.A.cuda()
     B = prob.B.cuda()
-    D = torch.empty(wl.M, wl.N, dtype=torch.float32, device="cuda")
-    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    SA = prob.scale_a.cuda() if prob.scale_a is not None else None
+    SB = prob.scale_b.cuda() if prob.scale_b is not None else None
+    dshape = (wl.batch, wl.M, wl.N) if wl.batch > 1 else (wl.M, wl.N)
+    D = torch.empty(dshape, dtype=tdt[wl.dtype_out], device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=code[wl.dtype_in], dtype_d=code[wl.dtype_out],
+                        scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128 if wl.block_scaled else dg.GEMM_SCALE_NONE)
     plan = dg.Plan(desc)
     info = plan.info.as_dict()
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
     flops = float(wl.flops)
+    nbytes = lambda t: 0 if t is None else t.numel() * t.element_size()  # noqa: E731
+    alg_bytes = float(nbytes(A) + nbytes(B) + nbytes(D) + nbytes(SA) + nbytes(SB))
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
 
     def step():
-        s = dg.gemm_run(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), None, None, sptr)
+        s = dg.gemm_run(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), ptr(SA), ptr(SB), sptr)
         if s != dg.GEMM_OK:
             raise dg.GemmError(s, "gemm_run")
 
@@ -267,30 +340,52 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = flops * world * args.steps / (total_ms / 1e3) / 1e12
 
-    # roofline of the dominant (only) kernel
-    peak, peak_sustained, peak_kind = peaks()
+    def metric_value(elapsed_ms, steps):
+        if winfo["unit"] == "GB/s":
+            return alg_bytes * world * steps / (elapsed_ms / 1e3) / 1e9
+        if winfo["unit"] == "us/launch":
+            return elapsed_ms * 1e3 / steps
+        return flops * world * steps / (elapsed_ms / 1e3) / 1e12
+
+    value = metric_value(total_ms, args.steps)
+
+    # roofline of the dominant (only) kernel, from its own launch events
+    peak_bf16, peak_bf16_sustained, peak_kind = peaks()
     mean_launch_ms = sum(launch_ms) / len(launch_ms)
-    achieved = flops / (mean_launch_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(),
-                "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
-                else "fallback 1900 TFLOP/s bf16",
-                "algorithmic_flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": float(wl.M * wl.K * 2 + wl.N * wl.K * 2 + wl.M * wl.N * 4)}
-    if peak_sustained:
-        roofline["frac_of_sustained"] = achieved / peak_sustained
+    if winfo["bound"] == "hbm":
+        hbm, kind = hbm_peak()
+        achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": None, "peak_kind": kind}
+    else:
+        peak = peak_bf16 * winfo["peak_ratio"]
+        achieved = flops / (mean_launch_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak,
+                    "traffic": profiled_traffic() if args.workload == WORKLOAD else None,
+                    "peak_kind": ("%s burst bf16 (MEASURED_PEAKS.json)%s" %
+                                  (peak_kind, " x 2 (fp8/bf16 nominal ratio 4.5/2.25)" if winfo["peak_ratio"] != 1 else ""))
+                    if peak_kind == "measured" else "fallback 1900 TFLOP/s bf16"}
+        if peak_bf16_sustained:
+            roofline["frac_of_sustained"] = achieved / (peak_bf16_sustained * winfo["peak_ratio"])
+        if winfo["bound"] == "latency":
+            roofline["bound"] = "tensor"
+            roofline["note"] = "launch-latency bound: 1 CTA; value is microseconds per launch"
+    roofline["algorithmic_flops_per_launch"] = flops
+    roofline["algorithmic_bytes_per_launch"] = alg_bytes
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     hA = prob.A.pin_memory()
     hB = prob.B.pin_memory()
-    hD = torch.empty(wl.M, wl.N, dtype=torch.float32).pin_memory()
+    hSA = prob.scale_a.pin_memory() if prob.scale_a is not None else None
+    hSB = prob.scale_b.pin_memory() if prob.scale_b is not None else None
+    hD = torch.empty(dshape, dtype=tdt[wl.dtype_out]).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        s = dg.gemm_run_host(plan.handle, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), None, None,
-                             A.data_ptr(), B.data_ptr(), D.data_ptr(), None, None, sptr)
+        s = dg.gemm_run_host(plan.handle, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), ptr(hSA), ptr(hSB),
+                             A.data_ptr(), B.data_ptr(), D.data_ptr(), ptr(SA), ptr(SB), sptr)
         if s != dg.GEMM_OK:
             raise dg.GemmError(s, "gemm_run_host")
 
@@ -310,32 +405,35 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e_value = flops * world * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_value = metric_value(e2e_ms, e2e_steps)
     st, rec = plan.sync_status()
     if st != dg.GEMM_OK:
         raise dg.GemmError(st, "e2e device status")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample, secs = cpu_oracle_sample(args.cpu_seconds, prob)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+        v, cores, sample, secs = cpu_oracle_sample(args.cpu_seconds, prob, winfo["unit"])
+        cpu = {"value": v, "unit": winfo["unit"], "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(secs, 2)}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s: D = A*B^T, M=N=K=8192, bf16 TN, fp32 accumulate, fp32 out" % WORKLOAD,
-                   "M": wl.M, "N": wl.N, "K": wl.K, "inputs": "U[-1,1] seed %d" % wl.seed,
+        "metric": winfo["metric"], "value": value, "unit": winfo["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": winfo["unit"] != "us/launch", "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype_in, "data": "synthetic",
+        "config": {"workload": "%s: %s" % (args.workload, winfo["text"]),
+                   "M": wl.M, "N": wl.N, "K": wl.K, "batch": wl.batch,
+                   "inputs": "%s seed %d" % (wl.dist, wl.seed),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "no flush: working set 537 MB > 129 MB L2",
+                   "l2": ("no flush: working set %.0f MB > 129 MB L2" % (alg_bytes / 1e6)) if alg_bytes > 129e6
+                   else "no flush: working set %.1f MB fits L2 (L2-warm)" % (alg_bytes / 1e6),
                    "plan": {k: info[k] for k in ("kernel", "cta_group", "tile_m", "tile_n", "tile_k", "stages",
                                                   "tmem_stages", "grid", "num_tiles", "smem_bytes")}},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
-                "h2d_bytes_per_step": int(hA.numel() * hA.element_size() + hB.numel() * hB.element_size()),
-                "d2h_bytes_per_step": int(hD.numel() * hD.element_size())},
+        "e2e": {"value": e2e_value, "unit": winfo["unit"], "steps": e2e_steps,
+                "h2d_bytes_per_step": int(nbytes(hA) + nbytes(hB) + nbytes(hSA) + nbytes(hSB)),
+                "d2h_bytes_per_step": int(nbytes(hD))},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "launch_ms": {"mean": mean_launch_ms, "min": min(launch_ms), "max": max(launch_ms),
@@ -355,6 +453,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_INFO), default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

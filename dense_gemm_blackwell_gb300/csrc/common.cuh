@@ -59,9 +59,10 @@ struct PersistentParams {
     CUtensorMap tmap_b;   // B: (K, N[, batch]) box (tile_k, tile_n / cta_group[, 1])
     CUtensorMap tmap_d;   // D: (N, M[, batch]) box (128 B of columns, 32[, 1])
     gemm_device_error_t* status;
-    const float* scale_a; // block-scaled kernels only
+    const float* scale_a; // block-scaled kernels only: [b][m][k/128] and [b][n/128][k/128]
     const float* scale_b;
     int64_t ld_sa, ld_sb;
+    int64_t stride_sa, stride_sb;
     int32_t M, N, K, batch;
     int32_t num_m_blocks, num_n_blocks, num_k_blocks;
     int32_t tiles_per_batch, num_tiles;

@@ -136,6 +136,59 @@ bool single_fits(const gemm_desc_t& d) {
     return d.M <= 128 && d.N <= 256 && d.K <= 256 && is16(d.dtype_a) && d.scale_mode == GEMM_SCALE_NONE;
 }
 
+// Block-scaled e4m3: 256-column tiles (two 128-column halves, each one 128-row
+// block of B's scales), 128-deep K stages, two TMEM partial buffers of 256
+// columns, 8 promotion/epilogue warps with one 4 KB staging buffer each.
+constexpr int kFp8Threads = 320;
+constexpr int64_t kFp8StagingBytes = 8 * 32 * 128;
+
+int choose_cta_group(const gemm_desc_t& d, const gemm_device_props_t& props, int64_t tile_n) {
+    if (d.flags & GEMM_FLAG_CTA_GROUP_1) return 1;
+    if (d.flags & GEMM_FLAG_CTA_GROUP_2) return 2;
+    // An SM pair halves each SM's B traffic; use it when there are enough pair
+    // tiles to occupy the GPU.
+    const int64_t pair_tiles = ceil_div(d.M, 256) * ceil_div(d.N, tile_n) * d.batch;
+    return (d.M > 128 && pair_tiles >= props.sm_count / 2) ? 2 : 1;
+}
+
+gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
+    if (d.tile_n != 0 && d.tile_n != 256) return GEMM_ERR_UNSUPPORTED;
+    const int64_t tile_n = 256;
+    const int cg = choose_cta_group(d, props, tile_n);
+    const int tile_k = 128;
+    const int64_t stage_bytes = 128 * tile_k + (tile_n / cg) * tile_k;
+    auto smem_for = [&](int64_t s) {
+        return s * stage_bytes + kFp8StagingBytes + 8 * (2 * s + 4 + 1) + 8 + kAlignSlack;
+    };
+    int64_t stages = d.stages;
+    if (stages == 0) {
+        stages = 16;
+        while (stages > 2 && smem_for(stages) > props.smem_optin_bytes) --stages;
+    }
+    if (stages < 2 || stages > 16) return GEMM_ERR_UNSUPPORTED;
+    if (smem_for(stages) > props.smem_optin_bytes) return GEMM_ERR_RESOURCES;
+    const int64_t tiles = ceil_div(d.M, 128 * cg) * ceil_div(d.N, tile_n) * d.batch;
+    if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    int64_t clusters = props.sm_count / cg;
+    if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
+    clusters = std::min<int64_t>(clusters, tiles);
+    info->kernel = GEMM_KERNEL_FP8_BLOCK;
+    info->cta_group = cg;
+    info->tile_m = 128 * cg;
+    info->tile_n = (int32_t)tile_n;
+    info->tile_k = tile_k;
+    info->stages = (int32_t)stages;
+    info->tmem_stages = 2;
+    info->tmem_cols = 512;
+    info->grid = (int32_t)(clusters * cg);
+    info->block_threads = kFp8Threads;
+    info->num_tiles = tiles;
+    info->stage_bytes = stage_bytes;
+    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * 2) + 4;
+    info->smem_bytes = smem_for(stages);
+    return GEMM_OK;
+}
+
 gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
     std::memset(info, 0, sizeof(*info));
     if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
@@ -143,8 +196,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if (is16(d.dtype_a)) {
         if (d.scale_mode != GEMM_SCALE_NONE) return GEMM_ERR_UNSUPPORTED;
     } else if (d.dtype_a == GEMM_E4M3) {
-        // block-scaled fp8 is planned by its own kernel family (not built in this version)
-        return GEMM_ERR_UNSUPPORTED;
+        if (d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128) return GEMM_ERR_UNSUPPORTED;
     } else {
         return GEMM_ERR_UNSUPPORTED;
     }
@@ -166,20 +218,12 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     }
     if (allow_single && single_fits(d)) return plan_single(d, props, info);
 
-    // ------------------------------------------------ persistent pipeline
+    // ------------------------------------------------ persistent pipelines
     if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
+    if (d.dtype_a == GEMM_E4M3) return plan_fp8(d, props, info);
     const int out_bytes = elem_bytes(d.dtype_d);
     const int chunk_cols = 128 / out_bytes;
-    int cg;
-    if (d.flags & GEMM_FLAG_CTA_GROUP_1) cg = 1;
-    else if (d.flags & GEMM_FLAG_CTA_GROUP_2) cg = 2;
-    else {
-        // An SM pair halves each SM's B traffic; use it when there are enough
-        // pair tiles to occupy the GPU.
-        const int64_t tn = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
-        const int64_t pair_tiles = ceil_div(d.M, 256) * ceil_div(d.N, tn) * d.batch;
-        cg = (d.M > 128 && pair_tiles >= props.sm_count / 2) ? 2 : 1;
-    }
+    const int cg = choose_cta_group(d, props, d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64));
     int64_t tile_n = d.tile_n;
     if (tile_n == 0) tile_n = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
     if (tile_n % 16 != 0 || tile_n < 16 || tile_n > 256) return GEMM_ERR_UNSUPPORTED;
@@ -279,6 +323,21 @@ bool encode_map(CUtensorMap* m, int dt, const void* base, int64_t cols, int64_t 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A persistent grid must be co-resident: cap it by the clusters the device can
+// hold at once with the chosen kernel's shared memory.
+gemm_status_t cap_resident(const gemm_desc_t& d, gemm_plan_info_t* info) {
+    int resident;
+    if (info->kernel == GEMM_KERNEL_PERSISTENT)
+        resident = dgb::persistent_max_active_clusters(info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
+    else if (info->kernel == GEMM_KERNEL_FP8_BLOCK)
+        resident = dgb::fp8_max_active_clusters(info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
+    else
+        return GEMM_OK;
+    if (resident <= 0) return cuda_fail(cudaGetLastError());
+    if (info->grid > resident * info->cta_group) info->grid = resident * info->cta_group;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- allocation-free variant state
@@ -360,14 +419,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
     gemm_plan_info_t info;
     s = plan(r.d, props, &info);
     if (s != GEMM_OK) return s;
-    if (info.kernel == GEMM_KERNEL_PERSISTENT) {
-        // A persistent grid must be co-resident: cap it by the clusters the
-        // device can hold at once with this kernel's shared memory.
-        const int resident = dgb::persistent_max_active_clusters(info.cta_group, r.d.dtype_d,
-                                                                 (size_t)info.smem_bytes);
-        if (resident <= 0) return cuda_fail(cudaGetLastError());
-        if (info.grid > resident * info.cta_group) info.grid = resident * info.cta_group;
-    }
+    if ((s = cap_resident(r.d, &info)) != GEMM_OK) return s;
     gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
     if (!p) return GEMM_ERR_RESOURCES;
     p->desc = r.d;
@@ -433,7 +485,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
         return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
     }
 
-    // persistent pipeline
+    if (scaled && (!aligned16(scale_a) || !aligned16(scale_b))) return GEMM_ERR_ALIGNMENT;
+
+    // persistent pipelines
     PersistentParams p;
     std::memset(&p, 0, sizeof(p));
     const int cg = info.cta_group;
@@ -463,7 +517,18 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
     p.flags = d.flags;
     p.timeout_ns = d.wait_timeout_ns;
-    e = dgb::launch_persistent(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
+    if (info.kernel == GEMM_KERNEL_FP8_BLOCK) {
+        p.scale_a = scale_a;
+        p.scale_b = scale_b;
+        p.ld_sa = d.ld_sa;
+        p.ld_sb = d.ld_sb;
+        p.stride_sa = d.stride_sa;
+        p.stride_sb = d.stride_sb;
+        p.idesc = dgb::make_idesc(0u /* e4m3 */, (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+        e = dgb::launch_fp8_block(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
+    } else {
+        e = dgb::launch_persistent(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
+    }
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
@@ -544,12 +609,7 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
     if (p.props.cc_major != 10 || p.props.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
     s = plan(r.d, p.props, &p.info);
     if (s != GEMM_OK) return s;
-    if (p.info.kernel == GEMM_KERNEL_PERSISTENT) {
-        const int resident = dgb::persistent_max_active_clusters(p.info.cta_group, r.d.dtype_d,
-                                                                 (size_t)p.info.smem_bytes);
-        if (resident <= 0) return cuda_fail(cudaGetLastError());
-        if (p.info.grid > resident * p.info.cta_group) p.info.grid = resident * p.info.cta_group;
-    }
+    if ((s = cap_resident(r.d, &p.info)) != GEMM_OK) return s;
     void* record = nullptr;
     if ((s = noalloc_address(dev, &record)) != GEMM_OK) return s;
     p.desc = r.d;

@@ -1,0 +1,303 @@
+// kernels_fp8.cu -- persistent tcgen05 GEMM for block-scaled e4m3 inputs.
+//
+//   D[m][n] = sum_kb  sA[m][kb] * sB[n/128][kb] * sum_{k in block kb} qA[m][k] * qB[n][k]
+//
+// Every 1x128 block of a row of A and every 128x128 block of B carries its own
+// fp32 scale ("Hopper and Blackwell GEMM", concept "FP8 and FP4, with block
+// scaling").  Those scales are arbitrary fp32 values, which the hardware's
+// block-scaled MMA kinds (E8M0 scales per 32 elements) cannot express, so the
+// scales are applied in software, once per 128-deep K block:
+//
+//   warp 0, one lane : TMA producer (shared loop), one 128-deep K block per ring
+//                      stage (one 128-byte swizzle row of e4m3).
+//   warp 1           : allocates tensor memory; one lane of the pair leader
+//                      issues four K32 tcgen05.mma kind::f8f6f4 per block into a
+//                      fresh partial P[j mod 2] (j counts blocks over all tiles)
+//                      and commits it to the partial's full barrier.
+//   warps 2..9       : promotion and epilogue.  Warp w owns TMEM lanes
+//                      32*(w mod 4).. (its 32 rows) and 128 of the tile's 256
+//                      columns (half (w-2)/4, exactly one 128-row block of B).
+//                      Per block: read its 32x128 slice of P with tcgen05.ld,
+//                      give the partial back, and accumulate
+//                      acc += P * (sA[row][kb] * sB[col/128][kb]) in registers.
+//                      After the tile's last block: convert, stage in swizzled
+//                      shared memory, TMA store.
+//
+// Two partial buffers let the tensor core compute block j+1 while the
+// epilogue warps promote block j.  Waits are bounded as in the 16-bit kernel.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "common.cuh"
+#include "launch.h"
+#include "pipeline.cuh"
+
+namespace dgb {
+
+constexpr int kFp8TileK = 128;              // e4m3 elements per ring stage (128 B)
+constexpr int kFp8EpiWarps = 8;
+constexpr int kFp8Threads = 64 + 32 * kFp8EpiWarps;
+constexpr uint32_t kFp8StagingBytes = 32 * 128;   // one buffer per epilogue warp
+
+template <int CG, int OUT>
+__global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_constant__ PersistentParams p) {
+    constexpr int kOutBytes = (OUT == GEMM_F32) ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;          // columns per 128-byte staging row
+    constexpr int kChunks = 128 / kChunkCols;            // chunks per warp's 128 columns
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int S = p.stages;
+    const uint32_t stage_bytes = p.stage_bytes_a + p.stage_bytes_b;
+    uint8_t* ring = smem;
+    uint8_t* staging = ring + (size_t)S * stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kFp8EpiWarps * kFp8StagingBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4 + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8u * S;
+    const uint32_t pfull0 = empty0 + 8u * S;     // partial buffer written (2)
+    const uint32_t pempty0 = pfull0 + 16u;       // partial buffer read (2)
+    const uint32_t drain_bar = pempty0 + 16u;
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(pfull0 + 8u * j, 1);
+            mbar_init(pempty0 + 8u * j, CG * kFp8EpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&p.tmap_a);
+        prefetch_tensormap(&p.tmap_b);
+        prefetch_tensormap(&p.tmap_d);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int cluster_id = blockIdx.x / CG;
+    const int num_clusters = gridDim.x / CG;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        if (lane == 0)
+            producer_loop<CG>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank, cluster_id,
+                              num_clusters);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int pb = 0;
+            uint32_t pphase = 0;
+            bool aborted = false;
+            bool issued_any = false;
+            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase<CG == 2>(pempty0 + 8u * pb, pphase ^ 1u, abort_flag, tmo, p.status, kRoleMma,
+                                             pb, t)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!wait_phase<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma, stage,
+                                           t)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                    const uint64_t da = smem_desc_sw128(sa);
+                    const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
+#pragma unroll
+                    for (int kk = 0; kk < kFp8TileK / 32; ++kk)
+                        mma_f8<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, kk != 0);
+                    issued_any = true;
+                    commit_to<CG>(empty0 + 8u * stage);
+                    commit_to<CG>(pfull0 + 8u * pb);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (++pb == 2) { pb = 0; pphase ^= 1u; }
+                }
+            }
+            if (aborted && issued_any) {
+                commit_local<CG>(drain_bar);
+                wait_phase_drain(drain_bar, 0, tmo);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ promotion + epilogue
+        const int wq = warp & 3;                  // TMEM lane quarter
+        const int half = (warp - 2) >> 2;         // which 128 columns of the tile
+        uint8_t* buf = staging + (warp - 2) * kFp8StagingBytes;
+        int pb = 0;
+        uint32_t pphase = 0;
+        bool aborted = false;
+        for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+            int b, mb, nb;
+            tile_coords(p, t, b, mb, nb);
+            const int m_warp = mb * (128 * CG) + (int)rank * 128 + wq * 32;
+            const int row = m_warp + lane;
+            const int col0 = nb * p.tile_n + half * 128;
+            const bool row_ok = row < p.M;
+            const bool cols_ok = col0 < p.N;
+            const float* sa_row = p.scale_a + (size_t)b * p.stride_sa + (size_t)(row_ok ? row : 0) * p.ld_sa;
+            const float* sb_blk = p.scale_b + (size_t)b * p.stride_sb + (size_t)(cols_ok ? col0 / 128 : 0) * p.ld_sb;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                const float s = (row_ok && cols_ok) ? __ldg(sa_row + kb) * __ldg(sb_blk + kb) : 0.0f;
+                int ok = 0;
+                if (lane == 0)
+                    ok = wait_phase<false>(pfull0 + 8u * pb, pphase, abort_flag, tmo, p.status, kRoleEpilogue, pb, t);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { aborted = true; break; }
+                tc_fence_after();
+                if (cols_ok) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(pb * p.tile_n + half * 128);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        tmem_wait_ld();
+                        tmem_reg_fence(r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 32 + i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_leader<CG>(pempty0 + 8u * pb);
+                if (++pb == 2) { pb = 0; pphase ^= 1u; }
+            }
+            if (aborted || !cols_ok || m_warp >= p.M) continue;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                uint32_t w[32];
+                if constexpr (OUT == GEMM_F32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(acc[c * 32 + i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = pack2<OUT>(acc[c * 64 + 2 * i], acc[c * 64 + 2 * i + 1]);
+                }
+                const int x = col0 + c * kChunkCols;
+                if (x >= p.N) break;
+                // single staging buffer: the previous store must have read it
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m_warp, b);
+                    else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m_warp);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+template <int CG, int OUT>
+static cudaLaunchConfig_t fp8_config(size_t smem, int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kFp8Threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int CG, int OUT>
+static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
+    auto kern = fp8_block_kernel<CG, OUT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, grid, stream, attr);
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int CG, int OUT>
+static int fp8_clusters_typed(size_t smem) {
+    auto kern = fp8_block_kernel<CG, OUT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, CG, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+#define DGB_FP8_DISPATCH(FN, ...)                                                        \
+    if (cta_group == 1) {                                                                \
+        switch (dtype_d) {                                                               \
+        case GEMM_F32: return FN<1, GEMM_F32>(__VA_ARGS__);                              \
+        case GEMM_BF16: return FN<1, GEMM_BF16>(__VA_ARGS__);                            \
+        case GEMM_F16: return FN<1, GEMM_F16>(__VA_ARGS__);                              \
+        default: break;                                                                  \
+        }                                                                                \
+    } else {                                                                             \
+        switch (dtype_d) {                                                               \
+        case GEMM_F32: return FN<2, GEMM_F32>(__VA_ARGS__);                              \
+        case GEMM_BF16: return FN<2, GEMM_BF16>(__VA_ARGS__);                            \
+        case GEMM_F16: return FN<2, GEMM_F16>(__VA_ARGS__);                              \
+        default: break;                                                                  \
+        }                                                                                \
+    }
+
+cudaError_t launch_fp8_block(const PersistentParams& p, int cta_group, int dtype_d, int grid, size_t smem_bytes,
+                             cudaStream_t stream) {
+    DGB_FP8_DISPATCH(fp8_launch_typed, p, grid, smem_bytes, stream)
+    return cudaErrorInvalidValue;
+}
+
+int fp8_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes) {
+    DGB_FP8_DISPATCH(fp8_clusters_typed, smem_bytes)
+    return 0;
+}
+
+}  // namespace dgb

@@ -41,6 +41,7 @@
 #include "ptx.cuh"
 #include "common.cuh"
 #include "launch.h"
+#include "pipeline.cuh"
 
 namespace dgb {
 
@@ -48,35 +49,6 @@ constexpr int kTileK16 = 64;               // K depth of one ring stage (16-bit 
 constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = 192;
-
-__device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, int& b, int& mb, int& nb) {
-    b = t / p.tiles_per_batch;
-    const int r = t - b * p.tiles_per_batch;
-    const int span = p.group_m * p.num_n_blocks;
-    const int g = r / span;
-    const int first_m = g * p.group_m;
-    const int gm = min(p.num_m_blocks - first_m, p.group_m);
-    const int rr = r - g * span;
-    mb = first_m + rr % gm;
-    nb = rr / gm;
-}
-
-template <int CG>
-__device__ __forceinline__ void commit_to(uint32_t bar) {
-    if constexpr (CG == 1) mma_commit(bar);
-    else mma_commit_pair(bar, 0x3);   // same barrier offset in both CTAs of the pair
-}
-
-template <int OUT>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if constexpr (OUT == GEMM_BF16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __half2 v = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&v);
-    }
-}
 
 template <int CG, int OUT>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_constant__ PersistentParams p) {
@@ -144,73 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued = 0;
-            bool aborted = false;
-            const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
-            const int b_rows = p.tile_n / CG;
-            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
-                int b, mb, nb;
-                tile_coords(p, t, b, mb, nb);
-                const int a_row = mb * (128 * CG) + (int)rank * 128;
-                const int b_row = nb * p.tile_n + (int)rank * b_rows;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!wait_phase<false>(empty(stage), phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
-                                           stage, t)) {
-                        aborted = true;
-                        break;
-                    }
-                    const uint32_t fb = (CG == 2) ? map_to_cta(full(stage), 0) : full(stage);
-                    if (leader) mbar_arrive_expect_tx(full(stage), tx_bytes);
-                    const bool drop = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0 && issued == 0;
-                    if (!drop) {
-                        const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                        const uint32_t sb = sa + p.stage_bytes_a;
-                        const int kx = kb * kTileK16;
-                        if constexpr (CG == 1) {
-                            if (p.batched) {
-                                tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
-                                tma_load_3d(sb, &p.tmap_b, fb, kx, b_row, b);
-                            } else {
-                                tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
-                                tma_load_2d(sb, &p.tmap_b, fb, kx, b_row);
-                            }
-                        } else {
-                            if (p.batched) {
-                                tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
-                                tma_load_3d_pair(sb, &p.tmap_b, fb, kx, b_row, b);
-                            } else {
-                                tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
-                                tma_load_2d_pair(sb, &p.tmap_b, fb, kx, b_row);
-                            }
-                        }
-                    }
-                    ++issued;
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
-            }
-            if (!aborted) {
-                // Tail: wait until the MMA released every slot, so that no commit
-                // arrives on this CTA's barriers after it exits.
-                for (int i = 0; i < S; ++i) {
-                    if (!wait_phase<false>(empty(stage), phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
-                                           stage, 0xFFFFFFFFu))
-                        break;
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
-            } else if (leader) {
-                // Abort: wait (bounded) for the copies still in flight into the ring.
-                int s = stage;
-                uint32_t ph = phase;
-                const int n = issued < S ? issued : S;
-                for (int i = 0; i < n; ++i) {
-                    if (s == 0) { s = S - 1; ph ^= 1u; } else { --s; }
-                    wait_phase_drain(full(s), ph, tmo);
-                }
-            }
-        }
+        if (lane == 0)
+            producer_loop<CG>(p, ring, stage_bytes, kTileK16, full0, empty0, abort_flag, rank, cluster_id,
+                              num_clusters);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -251,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             }
             if (aborted && issued_any) {
                 // Abort: make sure every MMA issued so far has finished before TMEM is freed.
-                if constexpr (CG == 1) mma_commit(drain_bar);
-                else mma_commit_pair(drain_bar, 0x1);
+                commit_local<CG>(drain_bar);
                 wait_phase_drain(drain_bar, 0, tmo);
             }
         }
@@ -284,10 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 // Every TMEM read of this tile by this warp is complete: hand the buffer back.
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if constexpr (CG == 1) mbar_arrive(tempty(acc));
-                    else mbar_arrive_remote(map_to_cta(tempty(acc), 0));
-                }
+                if (lane == 0) arrive_leader<CG>(tempty(acc));
             };
             if (n_valid == 0) release();
             for (int c = 0; c < n_valid; ++c) {

@@ -1,0 +1,143 @@
+// pipeline.cuh -- pieces shared by the persistent kernels: tile raster, the TMA
+// producer loop, MMA commits and output packing.
+//
+// The producer follows the main loop of "Hopper and Blackwell GEMM" (warp
+// specialisation): one thread walks every K slice of every tile the CTA (pair)
+// owns, waits for the ring slot to be empty, announces the slot's expected
+// bytes on its full barrier and issues the A and B tensor copies that complete
+// on it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "common.cuh"
+
+namespace dgb {
+
+// Linear tile index -> (batch, m block, n block); tiles of one batch entry are
+// visited in groups of `group_m` m blocks, n fastest inside a group's column,
+// so that the CTAs of one wave share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, int& b, int& mb, int& nb) {
+    b = t / p.tiles_per_batch;
+    const int r = t - b * p.tiles_per_batch;
+    const int span = p.group_m * p.num_n_blocks;
+    const int g = r / span;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.num_m_blocks - first_m, p.group_m);
+    const int rr = r - g * span;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+// Commit every MMA issued so far to `bar` (in both CTAs of a pair).
+template <int CG>
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+    if constexpr (CG == 1) mma_commit(bar);
+    else mma_commit_pair(bar, 0x3);
+}
+
+// Commit to `bar` of this CTA only (drain on the abort path).
+template <int CG>
+__device__ __forceinline__ void commit_local(uint32_t bar) {
+    if constexpr (CG == 1) mma_commit(bar);
+    else mma_commit_pair(bar, 0x1);
+}
+
+// Hand an accumulator (or partial) buffer back to the pair leader's MMA thread.
+template <int CG>
+__device__ __forceinline__ void arrive_leader(uint32_t bar) {
+    if constexpr (CG == 1) mbar_arrive(bar);
+    else mbar_arrive_remote(map_to_cta(bar, 0));
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (OUT == GEMM_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// TMA producer (one thread).  `tile_k` is the ring stage depth in elements of
+// A/B (one 128-byte swizzle row: 64 for 16-bit, 128 for 8-bit types).
+template <int CG>
+__device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes, int tile_k,
+                              uint32_t full0, uint32_t empty0, volatile uint32_t* abort_flag, uint32_t rank,
+                              int cluster_id, int num_clusters) {
+    const int S = p.stages;
+    const bool leader = rank == 0;
+    const uint64_t tmo = p.timeout_ns;
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool aborted = false;
+    const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
+    const int b_rows = p.tile_n / CG;
+    for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+        int b, mb, nb;
+        tile_coords(p, t, b, mb, nb);
+        const int a_row = mb * (128 * CG) + (int)rank * 128;
+        const int b_row = nb * p.tile_n + (int)rank * b_rows;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            const uint32_t empty_bar = empty0 + 8u * stage;
+            const uint32_t full_bar = full0 + 8u * stage;
+            if (!wait_phase<false>(empty_bar, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer, stage, t)) {
+                aborted = true;
+                break;
+            }
+            const uint32_t fb = (CG == 2) ? map_to_cta(full_bar, 0) : full_bar;
+            if (leader) mbar_arrive_expect_tx(full_bar, tx_bytes);
+            const bool drop = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0 && issued == 0;
+            if (!drop) {
+                const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                const uint32_t sb = sa + p.stage_bytes_a;
+                const int kx = kb * tile_k;
+                if constexpr (CG == 1) {
+                    if (p.batched) {
+                        tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
+                        tma_load_3d(sb, &p.tmap_b, fb, kx, b_row, b);
+                    } else {
+                        tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
+                        tma_load_2d(sb, &p.tmap_b, fb, kx, b_row);
+                    }
+                } else {
+                    if (p.batched) {
+                        tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
+                        tma_load_3d_pair(sb, &p.tmap_b, fb, kx, b_row, b);
+                    } else {
+                        tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
+                        tma_load_2d_pair(sb, &p.tmap_b, fb, kx, b_row);
+                    }
+                }
+            }
+            ++issued;
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+    }
+    if (!aborted) {
+        // Tail: wait until the MMA released every slot, so that no commit
+        // arrives on this CTA's barriers after it exits.
+        for (int i = 0; i < S; ++i) {
+            if (!wait_phase<false>(empty0 + 8u * stage, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
+                                   stage, 0xFFFFFFFFu))
+                break;
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+    } else if (leader) {
+        // Abort: wait (bounded) for the copies still in flight into the ring.
+        int s = stage;
+        uint32_t ph = phase;
+        const int n = issued < S ? issued : S;
+        for (int i = 0; i < n; ++i) {
+            if (s == 0) { s = S - 1; ph ^= 1u; } else { --s; }
+            wait_phase_drain(full0 + 8u * s, ph, tmo);
+        }
+    }
+}
+
+}  // namespace dgb

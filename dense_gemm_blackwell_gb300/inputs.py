@@ -129,12 +129,13 @@ def make(wl: Workload | str, *, seed: Optional[int] = None, dist: Optional[str] 
     if wl.batch != 1:
         raise ValueError("block-scaled workloads are single problems")
     if wl.dist == "ints":
-        # exact variant: small integers, power-of-two scales drawn per block
+        # exact variant: small integers and scales in {1/2, 1, 2}, so every block
+        # product, every scaled partial and every running sum is exact in fp32
         kb = (wl.K + 127) // 128
         qa = xa.to(torch.float8_e4m3fn)
         qb = xb.to(torch.float8_e4m3fn)
-        sa = torch.pow(2.0, torch.randint(-3, 4, (wl.M, kb), generator=gen).float())
-        sb = torch.pow(2.0, torch.randint(-3, 4, ((wl.N + 127) // 128, kb), generator=gen).float())
+        sa = torch.pow(2.0, torch.randint(-1, 2, (wl.M, kb), generator=gen).float())
+        sb = torch.pow(2.0, torch.randint(-1, 2, ((wl.N + 127) // 128, kb), generator=gen).float())
         return Problem(wl, qa.contiguous(), qb.contiguous(), sa.contiguous(), sb.contiguous())
     qa, sa = block_quantize_e4m3(xa, 1, 128)
     qb, sb = block_quantize_e4m3(xb, 128, 128)

@@ -140,3 +140,19 @@ def test_plan_create_without_device_fails_cleanly():
     assert s in (dg.GEMM_ERR_NO_DEVICE, dg.GEMM_ERR_CUDA)
     assert not h.value
     assert dg.gemm_plan_destroy(None) == dg.GEMM_OK
+
+
+def test_fp8_block_plan():
+    s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_BF16,
+                    scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    assert s == dg.GEMM_OK
+    assert info.kernel == dg.GEMM_KERNEL_FP8_BLOCK
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 128)
+    assert info.block_threads == 320 and info.tmem_cols == 512
+    assert info.smem_bytes <= GB300.smem_optin_bytes and info.stages >= 4
+    # e4m3 requires block scales; 16-bit inputs refuse them
+    s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
+    s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128,
+                 tile_n=128)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
