@@ -49,6 +49,7 @@ class GemmDesc(ctypes.Structure):
         ("stride_sa", ctypes.c_int64), ("stride_sb", ctypes.c_int64),
         ("flags", ctypes.c_uint32), ("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_uint64),
+        ("raster_group", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -216,7 +217,8 @@ def _torch_dtype(code):
 def make_desc(M, N, K, *, batch=1, dtype_a=GEMM_BF16, dtype_b=None, dtype_d=GEMM_F32,
               major_a=GEMM_K_MAJOR, major_b=GEMM_K_MAJOR, scale_mode=GEMM_SCALE_NONE,
               lda=0, ldb=0, ldd=0, stride_a=0, stride_b=0, stride_d=0, ld_sa=0, ld_sb=0,
-              stride_sa=0, stride_sb=0, flags=0, tile_n=0, stages=0, max_ctas=0, wait_timeout_ns=0) -> GemmDesc:
+              stride_sa=0, stride_sb=0, flags=0, tile_n=0, stages=0, max_ctas=0, wait_timeout_ns=0,
+              raster_group=0) -> GemmDesc:
     d = GemmDesc()
     d.M, d.N, d.K, d.batch = M, N, K, batch
     d.dtype_a = dtype_a
@@ -228,6 +230,7 @@ def make_desc(M, N, K, *, batch=1, dtype_a=GEMM_BF16, dtype_b=None, dtype_d=GEMM
     d.ld_sa, d.ld_sb, d.stride_sa, d.stride_sb = ld_sa, ld_sb, stride_sa, stride_sb
     d.flags, d.tile_n, d.stages, d.max_ctas = flags, tile_n, stages, max_ctas
     d.wait_timeout_ns = wait_timeout_ns
+    d.raster_group = raster_group
     return d
 
 

@@ -2,6 +2,7 @@
 // GEMM kernels (host and device).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -90,6 +91,28 @@ struct SingleParams {
     uint32_t idesc;
     uint64_t timeout_ns;
 };
+
+// ---------------------------------------------------------------- host helpers
+
+// Raise a kernel's dynamic shared-memory limit only when a launch needs more
+// than any earlier launch on this device did (the attribute call costs a
+// driver round trip; launches reuse the raised limit).
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, size_t smem, std::atomic<int> (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (done[dev].load(std::memory_order_acquire) >= (int)smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) {
+        int prev = done[dev].load();
+        while (prev < (int)smem && !done[dev].compare_exchange_weak(prev, (int)smem)) {}
+    }
+    return e;
+}
 
 // ---------------------------------------------------------------- bounded waits
 

@@ -254,7 +254,8 @@ static cudaLaunchConfig_t fp8_config(size_t smem, int grid, cudaStream_t stream,
 template <int CG, int OUT>
 static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = fp8_block_kernel<CG, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, grid, stream, attr);
@@ -264,7 +265,8 @@ static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t 
 template <int CG, int OUT>
 static int fp8_clusters_typed(size_t smem) {
     auto kern = fp8_block_kernel<CG, OUT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    static std::atomic<int> smem_set[kMaxDevices];
+    if (ensure_smem_limit(kern, smem, smem_set) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, CG, nullptr, attr);
     int n = 0;

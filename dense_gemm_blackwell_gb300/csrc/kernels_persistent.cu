@@ -250,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 template <int CG, int OUT>
 static cudaError_t launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = persistent_kernel<CG, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -270,7 +271,8 @@ static cudaError_t launch_typed(const PersistentParams& p, int grid, size_t smem
 template <int CG, int OUT>
 static int max_clusters_typed(size_t smem) {
     auto kern = persistent_kernel<CG, OUT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    static std::atomic<int> smem_set[kMaxDevices];
+    if (ensure_smem_limit(kern, smem, smem_set) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CG, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);

@@ -152,7 +152,8 @@ __global__ void zero_fill_kernel(void* D, int64_t M, int64_t N, int64_t batch, i
 template <int OUT>
 static cudaError_t launch_single_typed(const SingleParams& p, int batch, size_t smem, cudaStream_t stream) {
     auto kern = single_cta_kernel<OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<int> smem_set[kMaxDevices];
+    cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     kern<<<batch, 128, smem, stream>>>(p);
     return cudaGetLastError();

@@ -31,7 +31,8 @@
  * fallback to another kernel or to the CPU.
  *
  * Threading: calls on different plans are independent.  One plan may be run
- * on one stream at a time (its status record is shared by its launches).
+ * on one stream, from one host thread, at a time (its status record and its
+ * cached tensor maps are shared by its launches).
  */
 #ifndef DENSE_GEMM_BLACKWELL_GB300_GEMM_H
 #define DENSE_GEMM_BLACKWELL_GB300_GEMM_H
@@ -94,6 +95,8 @@ typedef struct {
     int32_t stages;             /* shared-memory ring depth (2..16); 0 = planner */
     int32_t max_ctas;           /* cap on persistent CTAs; 0 = all SMs */
     uint64_t wait_timeout_ns;   /* bound on every device-side wait; 0 = 2 s */
+    int32_t raster_group;       /* m blocks per raster group of the tile schedule; 0 = planner */
+    int32_t reserved0;          /* must be 0 */
 } gemm_desc_t;
 
 /* The planner's decisions, as gemm_plan_query / gemm_plan_info report them. */

@@ -91,6 +91,7 @@ def test_headline_plan_is_pair_tiles():
 def test_batched_plan():
     s, info = query(M=256, N=256, K=256, batch=512, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F16)
     assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT
+    assert info.cta_group == 1 and info.tile_n == 256   # short K: single-SM tiles
     assert info.num_tiles == 512 * (256 // info.tile_m) * (256 // info.tile_n)
 
 
@@ -147,7 +148,7 @@ def test_fp8_block_plan():
                     scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
     assert s == dg.GEMM_OK
     assert info.kernel == dg.GEMM_KERNEL_FP8_BLOCK
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 128)
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (1, 128, 256, 128)
     assert info.block_threads == 320 and info.tmem_cols == 512
     assert info.smem_bytes <= GB300.smem_optin_bytes and info.stages >= 4
     # e4m3 requires block scales; 16-bit inputs refuse them
