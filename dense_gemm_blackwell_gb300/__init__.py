@@ -33,6 +33,7 @@ GEMM_FLAG_CTA_GROUP_1 = 1 << 0
 GEMM_FLAG_CTA_GROUP_2 = 1 << 1
 GEMM_FLAG_NO_SINGLE_CTA = 1 << 2
 GEMM_FLAG_SINGLE_CTA = 1 << 3
+GEMM_FLAG_NO_L2_HINTS = 1 << 4
 GEMM_FLAG_TEST_DROP_LOAD = 1 << 30
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")

@@ -74,8 +74,12 @@ struct PersistentParams {
     uint32_t stage_bytes_a;   // per CTA
     uint32_t stage_bytes_b;   // per CTA
     uint32_t flags;
+    uint32_t l2_hints;        // bit 0: A loads evict_last; bit 1: D stores evict_first
     uint64_t timeout_ns;
 };
+
+constexpr uint32_t kHintKeepA = 1u;
+constexpr uint32_t kHintStreamD = 2u;
 
 // Single-CTA kernel: one CTA per batch entry, threads stage the operands.
 struct SingleParams {

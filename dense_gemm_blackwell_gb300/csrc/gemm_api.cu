@@ -39,7 +39,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kPersistentThreads = 192;
 constexpr int64_t kStagingBytes = 4 * 2 * 32 * 128;   // 4 epilogue warps x 2 buffers x 4 KB
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
-constexpr int kDefaultRasterGroup = 4;                 // m blocks per raster group (GB300 sweep, 8192^3)
+constexpr int kDefaultRasterGroup = 8;                 // m blocks per raster group (least DRAM traffic on GB300)
 
 thread_local int g_last_cuda_error = 0;
 
@@ -537,6 +537,10 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
     p.flags = d.flags;
     p.timeout_ns = d.wait_timeout_ns;
+    // Single long-K problems revisit A panels across the waves of a raster
+    // group and stream D out; batched problems touch every panel once.
+    p.l2_hints = (d.batch == 1 && p.num_k_blocks >= 8 && !(d.flags & GEMM_FLAG_NO_L2_HINTS))
+                     ? (dgb::kHintKeepA | dgb::kHintStreamD) : 0u;
     if (info.kernel == GEMM_KERNEL_FP8_BLOCK) {
         p.scale_a = scale_a;
         p.scale_b = scale_b;

@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
         __syncwarp();
     } else {
         // ------------------------------------------------------------ promotion + epilogue
+        // D is written once and never read back here: let it leave L2 first.
+        const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
+        const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                  // TMEM lane quarter
         const int half = (warp - 2) >> 2;         // which 128 columns of the tile
         uint8_t* buf = staging + (warp - 2) * kFp8StagingBytes;
@@ -217,8 +220,13 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m_warp, b);
-                    else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m_warp);
+                    if (stream_d) {
+                        if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m_warp, b, pol_d);
+                        else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m_warp, pol_d);
+                    } else {
+                        if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m_warp, b);
+                        else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m_warp);
+                    }
                     bulk_commit_group();
                 }
             }

@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // D is written once and never read back here: let it leave L2 first.
+        const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
+        const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                 // TMEM lanes [32*wq, 32*wq+32) are this warp's
         uint8_t* my_staging = staging + (warp - 2) * 2 * kStagingBytes;
         int acc = 0;
@@ -226,8 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0) {
                     const int x = n0 + c * kChunkCols;
-                    if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
-                    else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                    if (stream_d) {
+                        if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m0, b, pol_d);
+                        else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m0, pol_d);
+                    } else {
+                        if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
+                        else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                    }
                     bulk_commit_group();
                 }
                 ++stores;

@@ -17,8 +17,9 @@
 namespace dgb {
 
 // Linear tile index -> (batch, m block, n block); tiles of one batch entry are
-// visited in groups of `group_m` m blocks, n fastest inside a group's column,
-// so that the CTAs of one wave share A and B panels in L2.
+// visited in groups of `group_m` m blocks, m fastest inside a group, so that
+// the CTAs of one wave share A and B panels and consecutive waves of a group
+// share its A panels in L2.
 __device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, int& b, int& mb, int& nb) {
     b = t / p.tiles_per_batch;
     const int r = t - b * p.tiles_per_batch;
@@ -78,6 +79,9 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
     bool aborted = false;
     const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
     const int b_rows = p.tile_n / CG;
+    // Consecutive waves of a raster group reuse its A panels: keep them in L2.
+    const bool keep_a = (p.l2_hints & kHintKeepA) != 0;
+    const uint64_t pol_a = l2_policy_evict_last();
     for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
         int b, mb, nb;
         tile_coords(p, t, b, mb, nb);
@@ -99,18 +103,22 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 const int kx = kb * tile_k;
                 if constexpr (CG == 1) {
                     if (p.batched) {
-                        tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
+                        if (keep_a) tma_load_3d_hint(sa, &p.tmap_a, fb, kx, a_row, b, pol_a);
+                        else tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
                         tma_load_3d(sb, &p.tmap_b, fb, kx, b_row, b);
                     } else {
-                        tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
+                        if (keep_a) tma_load_2d_hint(sa, &p.tmap_a, fb, kx, a_row, pol_a);
+                        else tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
                         tma_load_2d(sb, &p.tmap_b, fb, kx, b_row);
                     }
                 } else {
                     if (p.batched) {
-                        tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
+                        if (keep_a) tma_load_3d_pair_hint(sa, &p.tmap_a, fb, kx, a_row, b, pol_a);
+                        else tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
                         tma_load_3d_pair(sb, &p.tmap_b, fb, kx, b_row, b);
                     } else {
-                        tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
+                        if (keep_a) tma_load_2d_pair_hint(sa, &p.tmap_a, fb, kx, a_row, pol_a);
+                        else tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
                         tma_load_2d_pair(sb, &p.tmap_b, fb, kx, b_row);
                     }
                 }

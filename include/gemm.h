@@ -75,6 +75,7 @@ typedef enum {
 #define GEMM_FLAG_CTA_GROUP_2     (1u << 1)  /* force the SM-pair (cta_group::2) MMA form */
 #define GEMM_FLAG_NO_SINGLE_CTA   (1u << 2)  /* never choose GEMM_KERNEL_SINGLE_CTA */
 #define GEMM_FLAG_SINGLE_CTA      (1u << 3)  /* require GEMM_KERNEL_SINGLE_CTA */
+#define GEMM_FLAG_NO_L2_HINTS     (1u << 4)  /* issue copies without L2 eviction-priority hints */
 #define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
                                                 the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
 
