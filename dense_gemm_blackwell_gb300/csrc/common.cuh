@@ -76,6 +76,15 @@ struct PersistentParams {
     uint32_t flags;
     uint32_t l2_hints;        // bit 0: A loads evict_last; bit 1: D stores evict_first
     uint64_t timeout_ns;
+    // Stream-K: the last sk_tiles tiles of the raster are split into equal K
+    // ranges over all clusters and processed first.  A contributor (the part
+    // of a tile that starts at K block 0) leaves its fp32 partial in
+    // sk_partials[slot] and publishes sk_flags = epoch; the finisher (the part
+    // that ends the tile) adds it before storing D.
+    int32_t sk_tiles;
+    uint32_t epoch;
+    float* sk_partials;       // [slot][cta rank][128 rows x tile_n], layout of sk_partial_index
+    uint32_t* sk_flags;       // [slot][cta rank][4 epilogue warps]
 };
 
 constexpr uint32_t kHintKeepA = 1u;
@@ -155,6 +164,33 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+// Bounded wait until a flag in global memory equals `value` (acquire, GPU
+// scope).  Same abort/timeout behaviour as wait_phase.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, volatile uint32_t* abort_flag,
+                                          uint64_t timeout_ns, gemm_device_error_t* st, uint32_t role,
+                                          uint32_t stage, uint32_t tile) {
+    auto probe = [&]() {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        return v == value;
+    };
+    if (probe()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (probe()) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            report_timeout(st, role, stage, tile);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void store_release_gpu(uint32_t* flag, uint32_t value) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(flag), "r"(value) : "memory");
 }
 
 // Wait that ignores the abort flag (used while draining in-flight copies on

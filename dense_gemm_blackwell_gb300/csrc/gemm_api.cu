@@ -194,6 +194,8 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
     return GEMM_OK;
 }
 
+void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info);
+
 gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
     std::memset(info, 0, sizeof(*info));
     if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
@@ -276,6 +278,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     info->stage_bytes = stage_bytes;
     info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * tmem_stages) + 4;
     info->smem_bytes = smem_for(stages);
+    plan_stream_k(d, info);
     return GEMM_OK;
 }
 
@@ -327,6 +330,28 @@ bool encode_map(CUtensorMap* m, int dt, const void* base, int64_t cols, int64_t 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stream-K for the 16-bit persistent kernel: when the tiles do not fill whole
+// waves of clusters, the last wave plus one full wave (sk_tiles >= clusters)
+// are split evenly along K over all clusters; the rest stays data-parallel.
+// Worth it only for long K (the fixup moves one fp32 tile per split).
+constexpr int kStreamKMinKBlocks = 16;
+
+void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
+    info->stream_k_tiles = 0;
+    info->workspace_bytes = 0;
+    if (info->kernel != GEMM_KERNEL_PERSISTENT || (d.flags & GEMM_FLAG_NO_STREAM_K)) return;
+    const int64_t clusters = info->grid / info->cta_group;
+    const int64_t nk = ceil_div(d.K, info->tile_k);
+    if (clusters < 2 || nk < kStreamKMinKBlocks || info->num_tiles < clusters) return;
+    const int64_t rem = info->num_tiles % clusters;
+    if (rem == 0) return;
+    info->stream_k_tiles = (int32_t)(clusters + rem);
+    // one partial slot per cluster: cta_group CTAs x 128 rows x tile_n fp32, plus 4 flags per CTA
+    const int64_t partial_bytes = clusters * info->cta_group * 128 * info->tile_n * 4;
+    const int64_t flag_bytes = round_up(clusters * info->cta_group * 4 * 4, 256);
+    info->workspace_bytes = partial_bytes + flag_bytes;
+}
 
 // A persistent grid must be co-resident: cap it by the clusters the device can
 // hold at once with the chosen kernel's shared memory.
@@ -391,7 +416,10 @@ struct gemm_plan_s {
     gemm_plan_info_t info;
     gemm_device_props_t props;
     int device;
-    gemm_device_error_t* status;  // device record
+    gemm_device_error_t* status;  // device record; stream-K flags and partials follow it
+    uint32_t* sk_flags;
+    float* sk_partials;
+    uint32_t epoch;               // launches so far (stream-K flags carry the launch's value)
 };
 
 extern "C" {
@@ -428,6 +456,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
     s = plan(r.d, props, &info);
     if (s != GEMM_OK) return s;
     if ((s = cap_resident(r.d, &info)) != GEMM_OK) return s;
+    plan_stream_k(r.d, &info);
     gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
     if (!p) return GEMM_ERR_RESOURCES;
     p->maps_valid = false;
@@ -436,14 +465,27 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
     p->props = props;
     p->device = dev;
     p->status = nullptr;
-    if ((e = cudaMalloc(&p->status, sizeof(gemm_device_error_t))) != cudaSuccess) {
+    p->sk_flags = nullptr;
+    p->sk_partials = nullptr;
+    p->epoch = 0;
+    // One allocation: status record (256 B), then stream-K flags, then partials.
+    const int64_t flag_bytes = info.stream_k_tiles
+                                   ? round_up((int64_t)(info.grid / info.cta_group) * info.cta_group * 16, 256) : 0;
+    const size_t total = 256 + (size_t)info.workspace_bytes;
+    void* mem = nullptr;
+    if ((e = cudaMalloc(&mem, total)) != cudaSuccess) {
         delete p;
         return cuda_fail(e);
     }
-    if ((e = cudaMemset(p->status, 0, sizeof(gemm_device_error_t))) != cudaSuccess) {
-        cudaFree(p->status);
+    if ((e = cudaMemset(mem, 0, 256 + (size_t)flag_bytes)) != cudaSuccess) {
+        cudaFree(mem);
         delete p;
         return cuda_fail(e);
+    }
+    p->status = static_cast<gemm_device_error_t*>(mem);
+    if (info.stream_k_tiles) {
+        p->sk_flags = reinterpret_cast<uint32_t*>(static_cast<char*>(mem) + 256);
+        p->sk_partials = reinterpret_cast<float*>(static_cast<char*>(mem) + 256 + flag_bytes);
     }
     *out = p;
     return GEMM_OK;
@@ -541,6 +583,13 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     // group and stream D out; batched problems touch every panel once.
     p.l2_hints = (d.batch == 1 && p.num_k_blocks >= 8 && !(d.flags & GEMM_FLAG_NO_L2_HINTS))
                      ? (dgb::kHintKeepA | dgb::kHintStreamD) : 0u;
+    if (info.stream_k_tiles > 0 && plan->sk_flags != nullptr) {
+        p.sk_tiles = info.stream_k_tiles;
+        p.epoch = ++plan->epoch;
+        if (p.epoch == 0) p.epoch = ++plan->epoch;   // 0 is the flags' initial value
+        p.sk_flags = plan->sk_flags;
+        p.sk_partials = plan->sk_partials;
+    }
     if (info.kernel == GEMM_KERNEL_FP8_BLOCK) {
         p.scale_a = scale_a;
         p.scale_b = scale_b;
@@ -634,6 +683,8 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
     s = plan(r.d, p.props, &p.info);
     if (s != GEMM_OK) return s;
     if ((s = cap_resident(r.d, &p.info)) != GEMM_OK) return s;
+    p.info.stream_k_tiles = 0;      // no workspace here: data-parallel tiles only
+    p.info.workspace_bytes = 0;
     void* record = nullptr;
     if ((s = noalloc_address(dev, &record)) != GEMM_OK) return s;
     p.desc = r.d;
@@ -653,7 +704,7 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     if (!plan) return GEMM_OK;
     cudaError_t e = cudaSuccess;
-    if (plan->status) e = cudaFree(plan->status);
+    if (plan->status) e = cudaFree(plan->status);   // one allocation holds the workspace too
     delete plan;
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }

@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             uint32_t acc_phase = 0;
             bool aborted = false;
             bool issued_any = false;
-            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+            WorkUnit u;
+            for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
+                const int t = u.tile;
                 if (!wait_phase<CG == 2>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma,
                                          acc, t)) {
                     aborted = true;
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
                         aborted = true;
                         break;
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
 #pragma unroll
                     for (int kk = 0; kk < kTileK16 / 16; ++kk)
-                        mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb | kk) != 0);
+                        mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
                     issued_any = true;
                     commit_to<CG>(empty(stage));
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -175,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         uint32_t acc_phase = 0;
         int stores = 0;                          // TMA stores issued; selects the staging buffer
         const int nchunks = p.tile_n / kChunkCols;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+        constexpr int kSub = kChunkCols / 32;    // 32-column TMEM loads per output chunk
+        WorkUnit u;
+        for (int idx = 0; next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
+            const int t = u.tile;
             int b, mb, nb;
             tile_coords(p, t, b, mb, nb);
             int ok = 0;
@@ -187,36 +192,90 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
             const int m0 = mb * (128 * CG) + (int)rank * 128 + wq * 32;
             const int n0 = nb * p.tile_n;
-            // Chunks that hold at least one in-range column of an in-range row; the
-            // rest of the tile (padding beyond M or N) is neither read nor stored.
-            const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
             auto release = [&]() {
                 // Every TMEM read of this tile by this warp is complete: hand the buffer back.
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive_leader<CG>(tempty(acc));
             };
+            const size_t part_base = (size_t)(u.slot * CG + (int)rank) * 128 * p.tile_n / 4;   // in float4
+            uint32_t* flag = p.sk_flags + (u.slot * CG + (int)rank) * 4 + wq;
+
+            if (u.role == kUnitContributor) {
+                // Leave this K range's fp32 partial for the finisher, then publish it.
+                float4* part = reinterpret_cast<float4*>(p.sk_partials) + part_base;
+                for (int c32 = 0; c32 < p.tile_n / 32; ++c32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_lane + c32 * 32, r);
+                    tmem_wait_ld();
+                    tmem_reg_fence(r);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        part[sk_partial_index(p.tile_n, wq, c32, j, lane)] =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                }
+                release();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) store_release_gpu(flag, p.epoch);
+                if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
+                continue;
+            }
+
+            const bool adds = u.role == kUnitFinisher;
+            if (adds) {
+                int got = 0;
+                if (lane == 0)
+                    got = wait_flag(flag, p.epoch, abort_flag, tmo, p.status, kRoleEpilogue, u.slot, t);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    release();
+                    break;
+                }
+                uint32_t v;   // every lane acquires the flag before reading the partial
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+                (void)v;
+            }
+            const float4* part = reinterpret_cast<const float4*>(p.sk_partials) + part_base;
+            // Chunks that hold at least one in-range column of an in-range row; the
+            // rest of the tile (padding beyond M or N) is neither read nor stored.
+            const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
             if (n_valid == 0) release();
             for (int c = 0; c < n_valid; ++c) {
                 uint32_t w[32];
-                if constexpr (OUT == GEMM_F32) {
-                    tmem_ld_32x32b_x32(t_lane + c * 32, w);
-                    tmem_wait_ld();
-                    tmem_reg_fence(w);
-                } else {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld_32x32b_x32(t_lane + c * 64, r0);
-                    tmem_ld_32x32b_x32(t_lane + c * 64 + 32, r1);
-                    tmem_wait_ld();
-                    tmem_reg_fence(r0);
-                    tmem_reg_fence(r1);
+                float f[32 * kSub];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        w[i] = pack2<OUT>(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-                        w[16 + i] = pack2<OUT>(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-                    }
+                for (int h = 0; h < kSub; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_lane + (c * kSub + h) * 32, r);
+                    tmem_wait_ld();
+                    tmem_reg_fence(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[h * 32 + i] = __uint_as_float(r[i]);
                 }
                 if (c == n_valid - 1) release();
+                if (adds) {
+#pragma unroll
+                    for (int h = 0; h < kSub; ++h) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 q = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                            // own part (later K) + partial (earlier K): one fixed order
+                            f[h * 32 + 4 * j] += q.x;
+                            f[h * 32 + 4 * j + 1] += q.y;
+                            f[h * 32 + 4 * j + 2] += q.z;
+                            f[h * 32 + 4 * j + 3] += q.w;
+                        }
+                    }
+                }
+                if constexpr (OUT == GEMM_F32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(f[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = pack2<OUT>(f[2 * i], f[2 * i + 1]);
+                }
                 // The staging buffer written two stores ago must have been read by that store.
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();

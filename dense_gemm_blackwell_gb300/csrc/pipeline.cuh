@@ -32,6 +32,65 @@ __device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, in
     nb = rr / gm;
 }
 
+// One piece of work of a cluster: K blocks [kb0, kb1) of one output tile.
+struct WorkUnit {
+    int tile;
+    int kb0, kb1;
+    int role;    // kUnitWhole, kUnitContributor or kUnitFinisher
+    int slot;    // partial slot written (contributor) or read (finisher)
+};
+constexpr int kUnitWhole = 0, kUnitContributor = 1, kUnitFinisher = 2;
+
+// The idx-th unit of cluster c (of G) in processing order.
+//  1. Stream-K region (tiles [T - sk_tiles, T)): its sk_tiles * nk K blocks
+//     are cut into G contiguous ranges, one per cluster.  Each range is at
+//     least one tile long (sk_tiles >= G), so a tile is split between at most
+//     two clusters: c-1 holds its start (contributor, slot c-1) and c its end
+//     (finisher).  A cluster walks its range from the last segment to the
+//     first: it publishes its contributor partial before anything else and
+//     reaches its finisher segment last, when c-1's partial is long done.
+//  2. Data-parallel tiles c, c+G, ... of [0, T - sk_tiles).
+__device__ __forceinline__ bool next_unit(const PersistentParams& p, int c, int G, int idx, WorkUnit& u) {
+    const int nk = p.num_k_blocks;
+    if (p.sk_tiles > 0) {
+        const int64_t total = (int64_t)p.sk_tiles * nk;
+        const int64_t it0 = total * c / G;
+        int64_t hi = total * (c + 1) / G;
+        int k = 0;
+        while (hi > it0) {
+            const int64_t j = (hi - 1) / nk;
+            const int64_t lo = it0 > j * nk ? it0 : j * nk;
+            if (k == idx) {
+                u.tile = p.num_tiles - p.sk_tiles + (int)j;
+                u.kb0 = (int)(lo - j * nk);
+                u.kb1 = (int)(hi - j * nk);
+                const bool starts = u.kb0 == 0, ends = u.kb1 == nk;
+                u.role = (starts && ends) ? kUnitWhole : (starts ? kUnitContributor : kUnitFinisher);
+                u.slot = starts ? c : c - 1;
+                return true;
+            }
+            ++k;
+            hi = lo;
+        }
+        idx -= k;
+    }
+    const int t = c + idx * G;
+    if (t >= p.num_tiles - p.sk_tiles) return false;
+    u.tile = t;
+    u.kb0 = 0;
+    u.kb1 = nk;
+    u.role = kUnitWhole;
+    u.slot = 0;
+    return true;
+}
+
+// Float4 index, inside one (slot, rank) partial, of 16-byte piece j (0..7) of
+// thread `lane` of epilogue warp wq for 32-column chunk c32: a warp's pieces
+// j are 512 contiguous bytes, so partial stores and loads are coalesced.
+__device__ __forceinline__ size_t sk_partial_index(int tile_n, int wq, int c32, int j, int lane) {
+    return ((size_t)(wq * (tile_n / 32) + c32) * 8 + j) * 32 + lane;
+}
+
 // Commit every MMA issued so far to `bar` (in both CTAs of a pair).
 template <int CG>
 __device__ __forceinline__ void commit_to(uint32_t bar) {
@@ -82,12 +141,14 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
     // Consecutive waves of a raster group reuse its A panels: keep them in L2.
     const bool keep_a = (p.l2_hints & kHintKeepA) != 0;
     const uint64_t pol_a = l2_policy_evict_last();
-    for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+    WorkUnit u;
+    for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
+        const int t = u.tile;
         int b, mb, nb;
         tile_coords(p, t, b, mb, nb);
         const int a_row = mb * (128 * CG) + (int)rank * 128;
         const int b_row = nb * p.tile_n + (int)rank * b_rows;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
             const uint32_t empty_bar = empty0 + 8u * stage;
             const uint32_t full_bar = full0 + 8u * stage;
             if (!wait_phase<false>(empty_bar, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer, stage, t)) {

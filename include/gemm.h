@@ -23,8 +23,10 @@
  *
  * Ownership: the caller owns every device buffer and the stream; the library
  * never frees or retains them past the call that uses them.  A plan owns its
- * host state and one small device status record (allocated by
- * gemm_plan_create, freed by gemm_plan_destroy).
+ * host state, one small device status record and, when the planner splits
+ * the last wave's tiles along K (stream-K), a workspace for fp32 partial
+ * tiles (all allocated by gemm_plan_create, freed by gemm_plan_destroy;
+ * gemm_plan_info reports its size).
  *
  * Errors: every call returns a gemm_status_t; nothing throws across the ABI.
  * Unsupported combinations fail with GEMM_ERR_UNSUPPORTED -- never a silent
@@ -76,6 +78,7 @@ typedef enum {
 #define GEMM_FLAG_NO_SINGLE_CTA   (1u << 2)  /* never choose GEMM_KERNEL_SINGLE_CTA */
 #define GEMM_FLAG_SINGLE_CTA      (1u << 3)  /* require GEMM_KERNEL_SINGLE_CTA */
 #define GEMM_FLAG_NO_L2_HINTS     (1u << 4)  /* issue copies without L2 eviction-priority hints */
+#define GEMM_FLAG_NO_STREAM_K     (1u << 5)  /* data-parallel tiles only (no stream-K workspace) */
 #define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
                                                 the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
 
@@ -116,6 +119,9 @@ typedef struct {
     int64_t stage_bytes;     /* bytes of one ring stage per CTA */
     int64_t pipeline_bytes;  /* ring + 8 B per barrier (2 per stage, 2 per TMEM stage) + 4 B TMEM handle */
     int64_t smem_bytes;      /* dynamic shared memory per CTA, all included */
+    int32_t stream_k_tiles;  /* tiles whose K range is split between two clusters (0 = data-parallel only) */
+    int32_t reserved;
+    int64_t workspace_bytes; /* device scratch the plan holds for stream-K partials and flags */
 } gemm_plan_info_t;
 
 /* Device properties the planner depends on (gemm_plan_query takes them explicitly). */

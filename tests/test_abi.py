@@ -157,3 +157,19 @@ def test_fp8_block_plan():
     s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128,
                  tile_n=128)
     assert s == dg.GEMM_ERR_UNSUPPORTED
+
+
+def test_stream_k_plan():
+    """Tiles that do not fill whole waves: the last wave plus one full wave are
+    split along K (stream-K), one fp32 partial slot per cluster."""
+    s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    assert s == dg.GEMM_OK
+    clusters = info.grid // info.cta_group
+    assert info.num_tiles % clusters != 0
+    assert info.stream_k_tiles == clusters + info.num_tiles % clusters
+    assert info.workspace_bytes >= clusters * info.cta_group * 128 * info.tile_n * 4
+    # whole waves, short K, or the flag: data-parallel only, no workspace
+    for kw in (dict(M=256 * 76, N=256, K=8192), dict(M=256, N=256, K=256, batch=512),
+               dict(M=8192, N=8192, K=8192, flags=dg.GEMM_FLAG_NO_STREAM_K)):
+        s, info = query(dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, **kw)
+        assert s == dg.GEMM_OK and info.stream_k_tiles == 0 and info.workspace_bytes == 0, kw

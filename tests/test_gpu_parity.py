@@ -136,6 +136,40 @@ def test_persistent_few_ctas_many_tiles():
     check_full(prob, "f32", exact=True, max_ctas=3, flags=dg.GEMM_FLAG_CTA_GROUP_1)
 
 
+@pytest.mark.parametrize("cg_flag,M,N,K,ctas,out", [
+    (dg.GEMM_FLAG_CTA_GROUP_2, 1024, 1024, 1024, 10, "f32"),
+    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 704, 1040, 8, "bf16"),
+    (dg.GEMM_FLAG_CTA_GROUP_1, 640, 768, 1152, 7, "f32"),
+    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 2064, 4, "f16"),
+])
+def test_stream_k_integers_bit_exact(cg_flag, M, N, K, ctas, out):
+    """Capping the clusters forces a partial last wave: its tiles are split
+    along K between two clusters (contributor partial + finisher)."""
+    prob = inputs.make("square8192_bf16", M=M, N=N, K=K, dist="ints", seed=17)
+    r, info = check_full(prob, out, exact=True, flags=cg_flag, max_ctas=ctas)
+    assert info["stream_k_tiles"] > 0
+
+
+def test_stream_k_matches_data_parallel():
+    prob = inputs.make("square4096_bf16", M=1024, N=768, K=2048, seed=18)
+    D1, info1 = run_gpu(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
+    D2, info2 = run_gpu(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_NO_STREAM_K, max_ctas=10)
+    assert info1["stream_k_tiles"] > 0 and info2["stream_k_tiles"] == 0
+    dref, s = oracle_rows(prob)
+    for D in (D1, D2):
+        assert compare(D.double().cpu().numpy().reshape(dref.shape), dref, s, "f32", TOL_16BIT)["ok"]
+    # repeated launches of one plan reuse the partial slots (flags carry a launch counter)
+    desc = dg.make_desc(prob.wl.M, prob.wl.N, prob.wl.K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32,
+                        flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
+    A, B = prob.A.cuda(), prob.B.cuda()
+    with dg.Plan(desc) as plan:
+        for _ in range(3):
+            D = torch.full_like(D1, float("nan"))
+            plan.run(A, B, D)
+            assert plan.sync_status()[0] == dg.GEMM_OK
+            assert torch.equal(D, D1)
+
+
 def test_persistent_batched_small():
     prob = inputs.make("batched256_f16", batch=7, seed=15)
     check_full(prob, "f16")
