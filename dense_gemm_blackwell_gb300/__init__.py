@@ -35,6 +35,8 @@ GEMM_FLAG_NO_SINGLE_CTA = 1 << 2
 GEMM_FLAG_SINGLE_CTA = 1 << 3
 GEMM_FLAG_NO_L2_HINTS = 1 << 4
 GEMM_FLAG_NO_STREAM_K = 1 << 5
+GEMM_FLAG_EPILOGUE_DIRECT = 1 << 6
+GEMM_FLAG_EPILOGUE_TMA = 1 << 7
 GEMM_FLAG_TEST_DROP_LOAD = 1 << 30
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
@@ -62,7 +64,7 @@ class GemmPlanInfo(ctypes.Structure):
         ("tmem_stages", ctypes.c_int32), ("tmem_cols", ctypes.c_int32), ("grid", ctypes.c_int32),
         ("block_threads", ctypes.c_int32), ("num_tiles", ctypes.c_int64), ("stage_bytes", ctypes.c_int64),
         ("pipeline_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
-        ("stream_k_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("stream_k_tiles", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self):

@@ -83,6 +83,12 @@ struct PersistentParams {
     // that ends the tile) adds it before storing D.
     int32_t sk_tiles;
     uint32_t epoch;
+    // Epilogue without shared-memory staging: each thread writes its row's
+    // 128-byte chunks straight to D (frees the staging area for a ring stage).
+    int32_t direct_store;
+    int32_t pad_;
+    void* d_ptr;
+    int64_t ldd, stride_d;
     float* sk_partials;       // [slot][cta rank][128 rows x tile_n], layout of sk_partial_index
     uint32_t* sk_flags;       // [slot][cta rank][4 epilogue warps]
 };

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     const uint32_t stage_bytes = p.stage_bytes_a + p.stage_bytes_b;
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kEpilogueWarps * 2 * kStagingBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + (p.direct_store ? 0 : kEpilogueWarps * 2 * kStagingBytes));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * TS + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -275,6 +275,33 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) w[i] = pack2<OUT>(f[2 * i], f[2 * i + 1]);
+                }
+                if (p.direct_store) {
+                    // This thread's row: 128 contiguous bytes, streaming stores.
+                    const int row = m0 + lane;
+                    const int x = n0 + c * kChunkCols;
+                    if (row < p.M) {
+                        uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
+                                       ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) * kOutBytes;
+                        if (x + kChunkCols <= p.N) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                __stcs(reinterpret_cast<int4*>(dst) + j,
+                                       make_int4((int)w[4 * j], (int)w[4 * j + 1], (int)w[4 * j + 2], (int)w[4 * j + 3]));
+                        } else {
+                            const int valid = p.N - x;
+#pragma unroll
+                            for (int e = 0; e < kChunkCols; ++e) {
+                                if (e < valid) {
+                                    if constexpr (OUT == GEMM_F32)
+                                        reinterpret_cast<uint32_t*>(dst)[e] = w[e];
+                                    else
+                                        reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+                                }
+                            }
+                        }
+                    }
+                    continue;
                 }
                 // The staging buffer written two stores ago must have been read by that store.
                 if (lane == 0) bulk_wait_group_read<1>();

@@ -79,6 +79,8 @@ typedef enum {
 #define GEMM_FLAG_SINGLE_CTA      (1u << 3)  /* require GEMM_KERNEL_SINGLE_CTA */
 #define GEMM_FLAG_NO_L2_HINTS     (1u << 4)  /* issue copies without L2 eviction-priority hints */
 #define GEMM_FLAG_NO_STREAM_K     (1u << 5)  /* data-parallel tiles only (no stream-K workspace) */
+#define GEMM_FLAG_EPILOGUE_DIRECT (1u << 6)  /* force direct row stores of D (no staging area) */
+#define GEMM_FLAG_EPILOGUE_TMA    (1u << 7)  /* force TMA stores of D through shared-memory staging */
 #define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
                                                 the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
 
@@ -120,7 +122,7 @@ typedef struct {
     int64_t pipeline_bytes;  /* ring + 8 B per barrier (2 per stage, 2 per TMEM stage) + 4 B TMEM handle */
     int64_t smem_bytes;      /* dynamic shared memory per CTA, all included */
     int32_t stream_k_tiles;  /* tiles whose K range is split between two clusters (0 = data-parallel only) */
-    int32_t reserved;
+    int32_t epilogue;        /* 0 = TMA stores through shared-memory staging, 1 = direct row stores */
     int64_t workspace_bytes; /* device scratch the plan holds for stream-K partials and flags */
 } gemm_plan_info_t;
 

@@ -123,6 +123,17 @@ def test_persistent_ragged(cg_flag, dtype_in, out):
     check_full(prob, out, flags=cg_flag)
 
 
+@pytest.mark.parametrize("mode", [dg.GEMM_FLAG_EPILOGUE_DIRECT, dg.GEMM_FLAG_EPILOGUE_TMA])
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+def test_epilogue_modes_ragged(mode, out):
+    """Direct row stores and TMA-staged stores write the same D, ragged edges included."""
+    prob = inputs.make("square8192_bf16", M=600, N=712, K=1088, dist="ints", seed=19)
+    r, info = check_full(prob, out, exact=True, flags=dg.GEMM_FLAG_CTA_GROUP_2 | mode)
+    assert info["epilogue"] == (1 if mode == dg.GEMM_FLAG_EPILOGUE_DIRECT else 0)
+    r, info = check_full(prob, out, exact=True, flags=dg.GEMM_FLAG_CTA_GROUP_2 | mode, max_ctas=8)
+    assert info["stream_k_tiles"] > 0
+
+
 @pytest.mark.parametrize("tile_n", [64, 128, 192, 256])
 def test_persistent_tile_widths(tile_n):
     prob = inputs.make("square8192_bf16", M=384, N=700, K=256, dist="ints", seed=13)
