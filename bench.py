@@ -40,6 +40,16 @@ KERNEL_SOURCES = ["dense_gemm_blackwell_gb300/csrc/kernels_persistent.cu",
                   "dense_gemm_blackwell_gb300/csrc/common.cuh"]
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's `value` (a job takes as long as its slowest rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
@@ -335,10 +345,7 @@ def run_ours(args):
     if st != dg.GEMM_OK:
         raise dg.GemmError(st, "timed-region device status")
 
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
 
     def metric_value(elapsed_ms, steps):
@@ -401,10 +408,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     e2e_value = metric_value(e2e_ms, e2e_steps)
     st, rec = plan.sync_status()
     if st != dg.GEMM_OK:

@@ -19,7 +19,7 @@ __all__ = [
     "build", "lib", "GemmError", "GemmDesc", "GemmPlanInfo", "GemmDeviceProps", "GemmDeviceError",
     "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host", "gemm_run_noalloc",
     "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
-    "gemm_version", "Plan", "matmul", "header_functions",
+    "gemm_version", "gemm_schedule_model", "gemm_schedule_choose", "Plan", "matmul", "header_functions",
 ]
 
 # ---------------------------------------------------------------- constants (include/gemm.h)
@@ -74,6 +74,17 @@ class GemmPlanInfo(ctypes.Structure):
 class GemmDeviceProps(ctypes.Structure):
     _fields_ = [("sm_count", ctypes.c_int32), ("smem_optin_bytes", ctypes.c_int32),
                 ("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32)]
+
+
+class GemmSchedParams(ctypes.Structure):
+    _fields_ = [("tiles", ctypes.c_int32), ("k_slices", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("accumulators", ctypes.c_int32), ("t_issue", ctypes.c_double), ("t_load", ctypes.c_double),
+                ("t_mma", ctypes.c_double), ("t_epi", ctypes.c_double)]
+
+
+class GemmSchedResult(ctypes.Structure):
+    _fields_ = [("run_length", ctypes.c_double), ("tensor_busy", ctypes.c_double),
+                ("steady_period", ctypes.c_double), ("stages_needed", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class GemmDeviceError(ctypes.Structure):
@@ -131,6 +142,12 @@ def lib():
                 L.gemm_status_string.argtypes = [st]
                 L.gemm_status_string.restype = ctypes.c_char_p
                 L.gemm_last_cuda_error.restype = st
+                L.gemm_schedule_model.argtypes = [ctypes.POINTER(GemmSchedParams), ctypes.POINTER(GemmSchedResult)]
+                L.gemm_schedule_model.restype = st
+                L.gemm_schedule_choose.argtypes = [ctypes.POINTER(GemmSchedParams), ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.c_double, ctypes.POINTER(ctypes.c_int32),
+                                                   ctypes.POINTER(ctypes.c_int32)]
+                L.gemm_schedule_choose.restype = st
                 L.gemm_version.restype = st
                 _lib = L
     return _lib
@@ -192,6 +209,23 @@ def gemm_plan_destroy(plan) -> int:
 
 def gemm_status_string(status) -> str:
     return lib().gemm_status_string(int(status)).decode()
+
+
+def gemm_schedule_model(tiles, k_slices, stages, accumulators, t_issue, t_load, t_mma, t_epi):
+    """Evaluate the pipeline schedule model; returns (status, GemmSchedResult)."""
+    p = GemmSchedParams(tiles, k_slices, stages, accumulators, t_issue, t_load, t_mma, t_epi)
+    r = GemmSchedResult()
+    return lib().gemm_schedule_model(ctypes.byref(p), ctypes.byref(r)), r
+
+
+def gemm_schedule_choose(tiles, k_slices, t_issue, t_load, t_mma, t_epi, max_stages, max_accumulators,
+                         tolerance=0.0):
+    """Fewest accumulators, then stages, within `tolerance` of the deepest pipeline: (status, S, A)."""
+    p = GemmSchedParams(tiles, k_slices, 1, 1, t_issue, t_load, t_mma, t_epi)
+    s, a = ctypes.c_int32(), ctypes.c_int32()
+    st = lib().gemm_schedule_choose(ctypes.byref(p), max_stages, max_accumulators, tolerance,
+                                    ctypes.byref(s), ctypes.byref(a))
+    return st, s.value, a.value
 
 
 def gemm_last_cuda_error() -> int:

@@ -237,6 +237,46 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
                                const float* scale_a, const float* scale_b, gemm_stream_t stream,
                                gemm_device_error_t* status_out);
 
+/* Inputs of the pipeline schedule model (time units are arbitrary but common). */
+typedef struct {
+    int32_t tiles;          /* T: output tiles one CTA runs in sequence */
+    int32_t k_slices;       /* K: ring stages (K slices) per tile */
+    int32_t stages;         /* S: shared-memory ring depth */
+    int32_t accumulators;   /* A: accumulator buffers (TMEM stages) */
+    double t_issue;         /* producer time to issue one slice's copies */
+    double t_load;          /* copy latency of one slice */
+    double t_mma;           /* tensor-core time of one slice */
+    double t_epi;           /* epilogue time of one tile */
+} gemm_sched_params_t;
+
+typedef struct {
+    double run_length;      /* end of the last tile's epilogue */
+    double tensor_busy;     /* T*K*t_mma / run_length */
+    double steady_period;   /* M_{g+S} - M_g over the last tile's last S slices (0 if K <= S) */
+    int32_t stages_needed;  /* ceil((t_load + t_mma) / t_mma): fewest stages that never starve */
+    int32_t reserved;
+} gemm_sched_result_t;
+
+/*
+ * gemm_schedule_model -- evaluate the max-plus schedule of a warp-specialised
+ * main loop ("Hopper and Blackwell GEMM", section "Maths"): with slices
+ * numbered g = t*K + k,
+ *   L_g = max(L_{g-1} + t_issue, D_{g-S}),
+ *   M_g = max(L_g + t_load, D_{g-1}, E_{t-A} if k = 0),
+ *   D_g = M_g + t_mma,  E_t = max(D_{tK+K-1}, E_{t-1}) + t_epi.
+ * Host arithmetic only.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG (counts below
+ * 1, T*K above 2^24, negative times, t_mma <= 0).
+ */
+gemm_status_t gemm_schedule_model(const gemm_sched_params_t* in, gemm_sched_result_t* out);
+
+/*
+ * gemm_schedule_choose -- the fewest accumulators, then the fewest stages,
+ * whose modelled run is within `tolerance` (relative) of the run with
+ * max_stages and max_accumulators; in->stages and in->accumulators are ignored.
+ */
+gemm_status_t gemm_schedule_choose(const gemm_sched_params_t* in, int32_t max_stages, int32_t max_accumulators,
+                                   double tolerance, int32_t* stages, int32_t* accumulators);
+
 /* gemm_plan_destroy -- free the plan and its status record (NULL is allowed). */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
