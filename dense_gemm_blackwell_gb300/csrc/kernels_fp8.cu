@@ -172,8 +172,19 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                const float s = (row_ok && cols_ok) ? __ldg(sa_row + kb) * __ldg(sb_blk + kb) : 0.0f;
+            // Scales are loaded two blocks ahead so that their L2 latency hides
+            // behind the promotion of the blocks in between.
+            const bool scaled = row_ok && cols_ok;
+            const int nkb = p.num_k_blocks;
+            float sa0 = scaled ? __ldg(sa_row) : 0.0f, sb0 = scaled ? __ldg(sb_blk) : 0.0f;
+            float sa1 = (scaled && nkb > 1) ? __ldg(sa_row + 1) : 0.0f;
+            float sb1 = (scaled && nkb > 1) ? __ldg(sb_blk + 1) : 0.0f;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const float s = sa0 * sb0;
+                sa0 = sa1;
+                sb0 = sb1;
+                sa1 = (scaled && kb + 2 < nkb) ? __ldg(sa_row + kb + 2) : 0.0f;
+                sb1 = (scaled && kb + 2 < nkb) ? __ldg(sb_blk + kb + 2) : 0.0f;
                 int ok = 0;
                 if (lane == 0)
                     ok = wait_phase<false>(pfull0 + 8u * pb, pphase, abort_flag, tmo, p.status, kRoleEpilogue, pb, t);
@@ -182,14 +193,16 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 tc_fence_after();
                 if (cols_ok) {
                     const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(pb * p.tile_n + half * 128);
+                    // 16-column loads keep the register footprint within what a
+                    // 10-warp CTA can hold (3 warps share a sub-partition's 16K registers).
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + c * 32, r);
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(taddr + c * 16, r);
                         tmem_wait_ld();
-                        tmem_reg_fence(r);
+                        tmem_reg_fence16(r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 32 + i]);
+                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 16 + i]);
                     }
                 }
                 tc_fence_before();
@@ -200,23 +213,26 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             if (aborted || !cols_ok || m_warp >= p.M) continue;
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
-                uint32_t w[32];
-                if constexpr (OUT == GEMM_F32) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(acc[c * 32 + i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = pack2<OUT>(acc[c * 64 + 2 * i], acc[c * 64 + 2 * i + 1]);
-                }
                 const int x = col0 + c * kChunkCols;
                 if (x >= p.N) break;
                 // single staging buffer: the previous store must have read it
                 if (lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
+                // 16-byte piece j of this thread's row, packed straight from the accumulators
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                for (int j = 0; j < 8; ++j) {
+                    uint4 q;
+                    if constexpr (OUT == GEMM_F32) {
+                        const int e = c * 32 + 4 * j;
+                        q = make_uint4(__float_as_uint(acc[e]), __float_as_uint(acc[e + 1]),
+                                       __float_as_uint(acc[e + 2]), __float_as_uint(acc[e + 3]));
+                    } else {
+                        const int e = c * 64 + 8 * j;
+                        q = make_uint4(pack2<OUT>(acc[e], acc[e + 1]), pack2<OUT>(acc[e + 2], acc[e + 3]),
+                                       pack2<OUT>(acc[e + 4], acc[e + 5]), pack2<OUT>(acc[e + 6], acc[e + 7]));
+                    }
+                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = q;
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
