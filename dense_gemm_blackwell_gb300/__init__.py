@@ -25,7 +25,7 @@ __all__ = [
 # ---------------------------------------------------------------- constants (include/gemm.h)
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE, GEMM_ERR_RESOURCES = 4, 5, 6, 7
-GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32 = 0, 1, 2, 3
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32, GEMM_E5M2, GEMM_TF32 = 0, 1, 2, 3, 4, 5
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
 GEMM_SCALE_NONE, GEMM_SCALE_BLOCK_1x128_128x128 = 0, 1
 GEMM_KERNEL_SINGLE_CTA, GEMM_KERNEL_PERSISTENT, GEMM_KERNEL_FP8_BLOCK, GEMM_KERNEL_ZERO_FILL = 1, 2, 3, 4
@@ -241,7 +241,7 @@ def gemm_version() -> int:
 def _dtype_code(t):
     import torch
     codes = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32,
-             torch.float8_e4m3fn: GEMM_E4M3}
+             torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}
     if t not in codes:
         raise TypeError("unsupported dtype %s" % t)
     return codes[t]
@@ -250,7 +250,7 @@ def _dtype_code(t):
 def _torch_dtype(code):
     import torch
     return {GEMM_F16: torch.float16, GEMM_BF16: torch.bfloat16, GEMM_F32: torch.float32,
-            GEMM_E4M3: torch.float8_e4m3fn}[code]
+            GEMM_E4M3: torch.float8_e4m3fn, GEMM_E5M2: torch.float8_e5m2}[code]
 
 
 def make_desc(M, N, K, *, batch=1, dtype_a=GEMM_BF16, dtype_b=None, dtype_d=GEMM_F32,
@@ -349,8 +349,11 @@ def matmul(a, b, *, out=None, out_dtype=None, scale_a=None, scale_b=None, flags=
         shape = (batch, M, N) if batched else (M, N)
         out = torch.empty(shape, dtype=_torch_dtype(code_d), device=a.device)
     da = _dtype_code(a.dtype)
-    desc = make_desc(M, N, K, batch=batch, dtype_a=da, dtype_b=_dtype_code(b.dtype), dtype_d=code_d,
-                     scale_mode=GEMM_SCALE_BLOCK_1x128_128x128 if da == GEMM_E4M3 else GEMM_SCALE_NONE,
+    db = _dtype_code(b.dtype)
+    if da == GEMM_F32:   # fp32 inputs are multiplied at tf32 precision
+        da = db = GEMM_TF32
+    desc = make_desc(M, N, K, batch=batch, dtype_a=da, dtype_b=db, dtype_d=code_d,
+                     scale_mode=GEMM_SCALE_BLOCK_1x128_128x128 if da in (GEMM_E4M3, GEMM_E5M2) else GEMM_SCALE_NONE,
                      lda=a.stride(-2), ldb=b.stride(-2), ldd=out.stride(-2),
                      stride_a=a.stride(0) if batched else 0, stride_b=b.stride(0) if batched else 0,
                      stride_d=out.stride(0) if batched else 0, flags=flags, tile_n=tile_n, stages=stages)

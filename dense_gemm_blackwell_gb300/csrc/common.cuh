@@ -43,11 +43,17 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t smem_addr) {
 //   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
 //   [15] A major (0 = K)       [16] B major      [17,23) N >> 3   [24,29) M >> 4
 // A/B format for kind::f16: 0 = f16, 1 = bf16; for kind::f8f6f4: 0 = e4m3.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m, uint32_t n,
-                                                  uint32_t a_mn_major = 0, uint32_t b_mn_major = 0) {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn_major << 15) |
+// kind::tf32: 2 = tf32.  kind::f8f6f4: 0 = e4m3, 1 = e5m2 (A and B independently).
+__host__ __device__ constexpr uint32_t make_idesc2(uint32_t a_format, uint32_t b_format, uint32_t m, uint32_t n,
+                                                   uint32_t a_mn_major = 0, uint32_t b_mn_major = 0) {
+    return (1u << 4) | (a_format << 7) | (b_format << 10) | (a_mn_major << 15) |
            (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m, uint32_t n,
+                                                  uint32_t a_mn_major = 0, uint32_t b_mn_major = 0) {
+    return make_idesc2(ab_format, ab_format, m, n, a_mn_major, b_mn_major);
+}
+constexpr uint32_t kMmaKindF16 = 0, kMmaKindTF32 = 1;
 
 // ---------------------------------------------------------------- parameters
 
@@ -70,6 +76,8 @@ struct PersistentParams {
     int32_t tile_n, stages, tmem_cols, tmem_stages;
     int32_t group_m;
     int32_t batched;          // 1 = 3-D tensor maps
+    int32_t tile_k;           // elements of K per ring stage (one 128-byte swizzle row)
+    uint32_t mma_kind;        // kMmaKindF16 or kMmaKindTF32 (16-bit kernel only)
     uint32_t idesc;
     uint32_t stage_bytes_a;   // per CTA
     uint32_t stage_bytes_b;   // per CTA

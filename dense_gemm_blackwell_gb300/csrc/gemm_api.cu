@@ -51,11 +51,13 @@ gemm_status_t cuda_fail(cudaError_t e) {
 int elem_bytes(int dt) {
     switch (dt) {
     case GEMM_F16: case GEMM_BF16: return 2;
-    case GEMM_E4M3: return 1;
-    case GEMM_F32: return 4;
+    case GEMM_E4M3: case GEMM_E5M2: return 1;
+    case GEMM_F32: case GEMM_TF32: return 4;
     default: return 0;
     }
 }
+
+bool is8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -199,12 +201,14 @@ void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info);
 
 gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
     std::memset(info, 0, sizeof(*info));
-    if (d.dtype_a != d.dtype_b) return GEMM_ERR_UNSUPPORTED;
     if (d.dtype_d != GEMM_F32 && d.dtype_d != GEMM_BF16 && d.dtype_d != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
-    if (is16(d.dtype_a)) {
-        if (d.scale_mode != GEMM_SCALE_NONE) return GEMM_ERR_UNSUPPORTED;
-    } else if (d.dtype_a == GEMM_E4M3) {
+    if (is8(d.dtype_a) && is8(d.dtype_b)) {
+        // e4m3 / e5m2 in any pairing, block-scaled only
         if (d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128) return GEMM_ERR_UNSUPPORTED;
+    } else if (d.dtype_a != d.dtype_b) {
+        return GEMM_ERR_UNSUPPORTED;
+    } else if (is16(d.dtype_a) || d.dtype_a == GEMM_TF32) {
+        if (d.scale_mode != GEMM_SCALE_NONE) return GEMM_ERR_UNSUPPORTED;
     } else {
         return GEMM_ERR_UNSUPPORTED;
     }
@@ -228,7 +232,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
 
     // ------------------------------------------------ persistent pipelines
     if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
-    if (d.dtype_a == GEMM_E4M3) return plan_fp8(d, props, info);
+    if (is8(d.dtype_a)) return plan_fp8(d, props, info);
     const int out_bytes = elem_bytes(d.dtype_d);
     const int chunk_cols = 128 / out_bytes;
     const int cg = choose_cta_group(d, props, d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64));
@@ -242,9 +246,9 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if (tmem_need > 512) return GEMM_ERR_RESOURCES;
     const int tmem_cols = pow2_at_least(tmem_need);
 
-    const int tile_k = 64;  // 16-bit inputs: one 128-byte swizzle row
-    const int64_t stage_a = 128 * tile_k * 2;
-    const int64_t stage_b = (tile_n / cg) * tile_k * 2;
+    const int tile_k = 128 / elem_bytes(d.dtype_a);  // one 128-byte swizzle row: 64 16-bit or 32 tf32 elements
+    const int64_t stage_a = 128 * 128;              // 128 rows x 128 B
+    const int64_t stage_b = (tile_n / cg) * 128;
     const int64_t stage_bytes = stage_a + stage_b;
     // Epilogue: TMA stores through a 32 KB staging area (default), or direct
     // row stores with no staging (on request).  On GB300 the staging area's
@@ -319,7 +323,7 @@ CUtensorMapDataType tma_dtype(int dt) {
     switch (dt) {
     case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    case GEMM_F32: case GEMM_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
     }
 }
@@ -587,7 +591,11 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.tmem_stages = info.tmem_stages;
     p.group_m = d.raster_group > 0 ? d.raster_group : kDefaultRasterGroup;
     p.batched = d.batch > 1 ? 1 : 0;
-    p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : 0u, (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+    p.tile_k = info.tile_k;
+    p.mma_kind = d.dtype_a == GEMM_TF32 ? dgb::kMmaKindTF32 : dgb::kMmaKindF16;
+    // A/B formats: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = tf32
+    p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u),
+                              (uint32_t)info.tile_m, (uint32_t)info.tile_n);
     p.stage_bytes_a = (uint32_t)(128 * info.tile_k * eb_a);
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
     p.flags = d.flags;
@@ -614,7 +622,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
         p.ld_sb = d.ld_sb;
         p.stride_sa = d.stride_sa;
         p.stride_sb = d.stride_sb;
-        p.idesc = dgb::make_idesc(0u /* e4m3 */, (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+        // kind::f8f6f4 formats: 0 = e4m3, 1 = e5m2
+        p.idesc = dgb::make_idesc2(d.dtype_a == GEMM_E5M2 ? 1u : 0u, d.dtype_b == GEMM_E5M2 ? 1u : 0u,
+                                   (uint32_t)info.tile_m, (uint32_t)info.tile_n);
         e = dgb::launch_fp8_block(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
     } else {
         e = dgb::launch_persistent(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);

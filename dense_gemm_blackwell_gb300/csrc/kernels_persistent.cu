@@ -45,7 +45,6 @@
 
 namespace dgb {
 
-constexpr int kTileK16 = 64;               // K depth of one ring stage (16-bit inputs: 128 B)
 constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = 192;
@@ -117,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0)
-            producer_loop<CG>(p, ring, stage_bytes, kTileK16, full0, empty0, abort_flag, rank, cluster_id,
+            producer_loop<CG>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
                               num_clusters);
         __syncwarp();
     } else if (warp == 1) {
@@ -148,9 +147,16 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                     const uint64_t da = smem_desc_sw128(sa);
                     const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
+                    // four MMAs per 128-byte row: K16 of 16-bit elements or K8 of tf32
+                    if (p.mma_kind == kMmaKindTF32) {
 #pragma unroll
-                    for (int kk = 0; kk < kTileK16 / 16; ++kk)
-                        mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_tf32<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
+                    }
                     issued_any = true;
                     commit_to<CG>(empty(stage));
                     if (++stage == S) { stage = 0; phase ^= 1u; }

@@ -34,7 +34,8 @@ import torch
 E4M3_MAX = 448.0
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
-                "e4m3": torch.float8_e4m3fn}
+                "tf32": torch.float32, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
 
 
 @dataclass
@@ -79,13 +80,14 @@ def _draw(shape, dist: str, gen: torch.Generator, K: int) -> torch.Tensor:
     raise ValueError(dist)
 
 
-def block_quantize_e4m3(x: torch.Tensor, block_rows: int, block_cols: int = 128):
-    """Quantise a 2-D fp32 matrix to E4M3 with one fp32 scale per block.
+def block_quantize_e4m3(x: torch.Tensor, block_rows: int, block_cols: int = 128, fmt: str = "e4m3"):
+    """Quantise a 2-D fp32 matrix to an 8-bit format with one fp32 scale per block.
 
-    scale = absmax(block) / 448 (1 for an all-zero block), q = e4m3(x / scale)
-    using torch's round-to-nearest cast.  Returns (q, scales) with scales of
-    shape (ceil(R/block_rows), ceil(C/block_cols)).
+    scale = absmax(block) / max_finite (448 for E4M3, 57344 for E5M2; 1 for an
+    all-zero block), q = fmt(x / scale) using torch's round-to-nearest cast.
+    Returns (q, scales) with scales of shape (ceil(R/block_rows), ceil(C/block_cols)).
     """
+    fmax = FP8_MAX[fmt]
     R, C = x.shape
     rb = (R + block_rows - 1) // block_rows
     cb = (C + block_cols - 1) // block_cols
@@ -93,9 +95,9 @@ def block_quantize_e4m3(x: torch.Tensor, block_rows: int, block_cols: int = 128)
     pad[:R, :C] = x
     blocks = pad.view(rb, block_rows, cb, block_cols)
     amax = blocks.abs().amax(dim=(1, 3))
-    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    scale = torch.where(amax > 0, amax / fmax, torch.ones_like(amax))
     scaled = blocks / scale[:, None, :, None]
-    q = scaled.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    q = scaled.clamp(-fmax, fmax).to(TORCH_DTYPES[fmt])
     q = q.view(rb * block_rows, cb * block_cols)[:R, :C].contiguous()
     return q, scale.contiguous()
 
@@ -112,12 +114,15 @@ class Problem:
 
 def make(wl: Workload | str, *, seed: Optional[int] = None, dist: Optional[str] = None,
          M: Optional[int] = None, N: Optional[int] = None, K: Optional[int] = None,
-         batch: Optional[int] = None) -> Problem:
-    """Draw the inputs of a workload (optionally at another size, seed or value mix)."""
+         batch: Optional[int] = None, dtype_in: Optional[str] = None,
+         dtype_b: Optional[str] = None) -> Problem:
+    """Draw the inputs of a workload (optionally at another size, seed, value mix or
+    input type; dtype_b sets B's type separately for 8-bit pairings)."""
     if isinstance(wl, str):
         wl = WORKLOADS[wl]
-    wl = Workload(wl.name, M or wl.M, N or wl.N, K or wl.K, batch or wl.batch, wl.dtype_in,
+    wl = Workload(wl.name, M or wl.M, N or wl.N, K or wl.K, batch or wl.batch, dtype_in or wl.dtype_in,
                   wl.dtype_out, dist or wl.dist, wl.seed if seed is None else seed, wl.block_scaled)
+    wl.extra["dtype_b"] = dtype_b or wl.dtype_in
     gen = torch.Generator().manual_seed(wl.seed)
     shape_a = (wl.batch, wl.M, wl.K) if wl.batch > 1 else (wl.M, wl.K)
     shape_b = (wl.batch, wl.N, wl.K) if wl.batch > 1 else (wl.N, wl.K)
@@ -125,20 +130,20 @@ def make(wl: Workload | str, *, seed: Optional[int] = None, dist: Optional[str] 
     xb = _draw(shape_b, wl.dist, gen, wl.K)
     if not wl.block_scaled:
         t = TORCH_DTYPES[wl.dtype_in]
-        return Problem(wl, xa.to(t).contiguous(), xb.to(t).contiguous())
+        return Problem(wl, xa.to(t).contiguous(), xb.to(TORCH_DTYPES[wl.extra["dtype_b"]]).contiguous())
     if wl.batch != 1:
         raise ValueError("block-scaled workloads are single problems")
     if wl.dist == "ints":
         # exact variant: small integers and scales in {1/2, 1, 2}, so every block
         # product, every scaled partial and every running sum is exact in fp32
         kb = (wl.K + 127) // 128
-        qa = xa.to(torch.float8_e4m3fn)
-        qb = xb.to(torch.float8_e4m3fn)
+        qa = xa.to(TORCH_DTYPES[wl.dtype_in])
+        qb = xb.to(TORCH_DTYPES[wl.extra["dtype_b"]])
         sa = torch.pow(2.0, torch.randint(-1, 2, (wl.M, kb), generator=gen).float())
         sb = torch.pow(2.0, torch.randint(-1, 2, ((wl.N + 127) // 128, kb), generator=gen).float())
         return Problem(wl, qa.contiguous(), qb.contiguous(), sa.contiguous(), sb.contiguous())
-    qa, sa = block_quantize_e4m3(xa, 1, 128)
-    qb, sb = block_quantize_e4m3(xb, 128, 128)
+    qa, sa = block_quantize_e4m3(xa, 1, 128, wl.dtype_in)
+    qb, sb = block_quantize_e4m3(xb, 128, 128, wl.extra["dtype_b"])
     return Problem(wl, qa, qb, sa, sb)
 
 

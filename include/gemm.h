@@ -60,7 +60,9 @@ typedef enum {
     GEMM_ERR_RESOURCES = 7     /* shared/tensor memory budget cannot hold the requested tile */
 } gemm_status_t;
 
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_F32 = 3 } gemm_dtype_t;
+/* Element types.  GEMM_TF32 is fp32 storage multiplied at tf32 precision (the
+ * tensor core reads the top 19 bits of each fp32 value); GEMM_F32 is an output type. */
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_F32 = 3, GEMM_E5M2 = 4, GEMM_TF32 = 5 } gemm_dtype_t;
 typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
 typedef enum { GEMM_SCALE_NONE = 0, GEMM_SCALE_BLOCK_1x128_128x128 = 1 } gemm_scale_mode_t;
 
@@ -88,7 +90,8 @@ typedef enum {
 typedef struct {
     int64_t M, N, K;        /* D is M x N per batch entry; K is the contraction length */
     int64_t batch;          /* number of independent problems (>= 1; 0 = no-op) */
-    int32_t dtype_a, dtype_b;   /* gemm_dtype_t: F16+F16, BF16+BF16, or E4M3+E4M3 (block-scaled) */
+    int32_t dtype_a, dtype_b;   /* gemm_dtype_t: F16+F16, BF16+BF16, TF32+TF32 (K-major), or any pair of
+                                   E4M3/E5M2 (block-scaled) */
     int32_t dtype_d;            /* gemm_dtype_t: F32, BF16 or F16 */
     int32_t major_a, major_b;   /* gemm_major_t */
     int32_t scale_mode;         /* gemm_scale_mode_t; BLOCK requires E4M3 inputs */

@@ -27,10 +27,11 @@ _lock = threading.Lock()
 _lib = None
 
 # element type codes of oracle.c
-F16, BF16, E4M3, F32 = 0, 1, 2, 3
+F16, BF16, E4M3, F32, E5M2 = 0, 1, 2, 3, 4
 _NAMES = {"f16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16,
-          "e4m3": E4M3, "float8_e4m3fn": E4M3, "f32": F32, "float32": F32}
-_BYTES = {F16: 2, BF16: 2, E4M3: 1, F32: 4}
+          "e4m3": E4M3, "float8_e4m3fn": E4M3, "f32": F32, "float32": F32,
+          "e5m2": E5M2, "float8_e5m2": E5M2}
+_BYTES = {F16: 2, BF16: 2, E4M3: 1, F32: 4, E5M2: 1}
 
 
 def dtype_code(name) -> int:

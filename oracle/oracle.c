@@ -35,6 +35,9 @@
  *   bf16  : 1 sign, 8 exponent (bias 127), 7 mantissa bits, IEEE inf/NaN
  *   e4m3  : 1 sign, 4 exponent (bias 7), 3 mantissa bits, no inf,
  *           S.1111.111 is NaN, largest finite 448 (OCP 8-bit FP, "E4M3FN")
+ *   e5m2  : 1 sign, 5 exponent (bias 15), 2 mantissa bits, IEEE inf/NaN,
+ *           largest finite 57344 (OCP 8-bit FP, "E5M2")
+ *   fp32  : 1 sign, 8 exponent (bias 127), 23 mantissa bits (also as an input)
  * Rounding to an output format is round-to-nearest, ties to even, from the
  * exact fp64 value (one rounding).  e4m3 encoding saturates to +-448.
  */
@@ -47,7 +50,7 @@
 #endif
 
 /* Element type codes used by this file's callers (the Python test wrapper). */
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F32 = 3 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F32 = 3, ORC_E5M2 = 4 };
 
 /* Parameters of one binary floating-point format. */
 typedef struct {
@@ -64,6 +67,7 @@ static int orc_format_of(int dtype, orc_format* f) {
     case ORC_BF16: f->mbits = 7;  f->ebits = 8; f->bias = 127; f->has_inf = 1; f->satfinite = 0; return 0;
     case ORC_F32:  f->mbits = 23; f->ebits = 8; f->bias = 127; f->has_inf = 1; f->satfinite = 0; return 0;
     case ORC_E4M3: f->mbits = 3;  f->ebits = 4; f->bias = 7;   f->has_inf = 0; f->satfinite = 1; return 0;
+    case ORC_E5M2: f->mbits = 2;  f->ebits = 5; f->bias = 15;  f->has_inf = 1; f->satfinite = 0; return 0;
     default: return -1;
     }
 }
@@ -174,7 +178,7 @@ void orc_encode_array(int dtype, const double* x, int64_t n, uint32_t* out) {
 static int orc_elem_bytes(int dtype) {
     switch (dtype) {
     case ORC_F16: case ORC_BF16: return 2;
-    case ORC_E4M3: return 1;
+    case ORC_E4M3: case ORC_E5M2: return 1;
     case ORC_F32: return 4;
     default: return 0;
     }
@@ -206,9 +210,11 @@ static int64_t orc_index_b(const orc_problem* p, int64_t b, int64_t n, int64_t k
     return b * p->stride_b + (p->major_b == 0 ? n * p->ldb + k : k * p->ldb + n);
 }
 
-/* Decode table for every code of an 8- or 16-bit format (filled from orc_decode). */
+/* Decode table for every code of an 8- or 16-bit format (filled from orc_decode);
+ * NULL for 32-bit formats, which are decoded element by element. */
 static double* orc_make_table(int dtype) {
     int bytes = orc_elem_bytes(dtype);
+    if (bytes > 2) return NULL;
     int64_t n = (int64_t)1 << (8 * bytes);
     double* t = (double*)malloc(sizeof(double) * (size_t)n);
     if (!t) return NULL;
@@ -217,15 +223,19 @@ static double* orc_make_table(int dtype) {
 }
 
 /* Real value of A(b,m,k) and B(b,n,k), scales applied when the problem is block-scaled. */
+static double orc_lookup(int dtype, const double* lut, uint32_t code) {
+    return lut ? lut[code] : orc_decode(dtype, code);
+}
+
 static double orc_value_a(const orc_problem* p, const double* lut, const void* A, const float* sA,
                           int64_t b, int64_t m, int64_t k) {
-    double v = lut[orc_load_code(A, orc_elem_bytes(p->dtype_a), orc_index_a(p, b, m, k))];
+    double v = orc_lookup(p->dtype_a, lut, orc_load_code(A, orc_elem_bytes(p->dtype_a), orc_index_a(p, b, m, k)));
     if (p->scaled) v *= (double)sA[b * p->stride_sa + m * p->ld_sa + k / 128];
     return v;
 }
 static double orc_value_b(const orc_problem* p, const double* lut, const void* B, const float* sB,
                           int64_t b, int64_t n, int64_t k) {
-    double v = lut[orc_load_code(B, orc_elem_bytes(p->dtype_b), orc_index_b(p, b, n, k))];
+    double v = orc_lookup(p->dtype_b, lut, orc_load_code(B, orc_elem_bytes(p->dtype_b), orc_index_b(p, b, n, k)));
     if (p->scaled) v *= (double)sB[b * p->stride_sb + (n / 128) * p->ld_sb + k / 128];
     return v;
 }
@@ -235,19 +245,19 @@ static double orc_value_b(const orc_problem* p, const double* lut, const void* B
  * row of D; row i of the outputs holds D_ref[b,m,0..N) and S[b,m,0..N).
  * rows == NULL means every row of every batch, in order.  Rows are spread
  * over OpenMP threads; each output element is one ascending-k fp64 sum.
- * Inputs are 8- or 16-bit codes.  Returns 0, or -1 on a bad argument.
+ * Inputs are 8-, 16- or 32-bit codes.  Returns 0, or -1 on a bad argument.
  */
 int orc_gemm_rows(const orc_problem* p, const void* A, const void* B,
                   const float* sA, const float* sB,
                   int64_t nrows, const int64_t* rows, double* dref, double* sabs) {
     if (!p || p->M < 0 || p->N < 0 || p->K < 0 || p->batch < 0) return -1;
     int ba = orc_elem_bytes(p->dtype_a), bb = orc_elem_bytes(p->dtype_b);
-    if (ba < 1 || ba > 2 || bb < 1 || bb > 2) return -1;
+    if (ba < 1 || bb < 1) return -1;
     if (p->scaled && (!sA || !sB)) return -1;
     if (rows == NULL) nrows = p->batch * p->M;
     double* lut_a = orc_make_table(p->dtype_a);
     double* lut_b = orc_make_table(p->dtype_b);
-    if (!lut_a || !lut_b) { free(lut_a); free(lut_b); return -1; }
+    if ((ba <= 2 && !lut_a) || (bb <= 2 && !lut_b)) { free(lut_a); free(lut_b); return -1; }
     const int64_t N = p->N, K = p->K;
 #pragma omp parallel
     {

@@ -7,7 +7,10 @@ Error metric (normalised by the per-element sum of |a||b|):
                     sum once: the two roundings can differ by one output ulp)
   S == 0          : D must be exactly 0
   integer inputs  : D == RNE(D_ref) bit for bit (every partial sum is exact in fp32)
-Tolerances: 2e-3 for 16-bit inputs, 2e-2 for block-scaled fp8.
+Tolerances: 2e-3 for 16-bit inputs, 2e-2 for block-scaled fp8, 4e-3 for tf32:
+the tensor core keeps 10 of fp32's 23 mantissa bits of each input, so each
+product may be off by up to about 2 * 2^-10 relative (2^-9 = 1.95e-3 of S),
+plus fp32 accumulation; 4e-3 leaves room for both.
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ import oracle
 
 TOL_16BIT = 2e-3
 TOL_FP8 = 2e-2
+TOL_TF32 = 4e-3
 MANTISSA = {"f32": 23, "bf16": 7, "f16": 10}
 MIN_NORMAL_EXP = {"f32": -126, "bf16": -126, "f16": -14}
 

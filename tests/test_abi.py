@@ -173,3 +173,16 @@ def test_stream_k_plan():
                dict(M=8192, N=8192, K=8192, flags=dg.GEMM_FLAG_NO_STREAM_K)):
         s, info = query(dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, **kw)
         assert s == dg.GEMM_OK and info.stream_k_tiles == 0 and info.workspace_bytes == 0, kw
+
+
+def test_variant_dtype_plans():
+    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and info.tile_k == 32
+    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, dtype_b=dg.GEMM_E5M2, dtype_d=dg.GEMM_BF16,
+                    scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_FP8_BLOCK
+    # tf32 is never handled by the thread-staged single-CTA kernel; 16/8-bit mixes are refused
+    s, info = query(M=64, N=64, K=64, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT
+    s, _ = query(M=64, N=64, K=64, dtype_a=dg.GEMM_BF16, dtype_b=dg.GEMM_E4M3)
+    assert s == dg.GEMM_ERR_UNSUPPORTED

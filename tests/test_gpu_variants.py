@@ -1,0 +1,87 @@
+"""GPU parity of the variant input types against the CPU oracle.
+
+tf32: fp32 storage multiplied at tf32 precision (kind::tf32, K = 8 per
+instruction).  Small integers are exact in tf32, so integer runs must match
+bit for bit; random inputs must stay within 4e-3 of S = sum |a||b| (the
+oracle uses the exact fp32 inputs; see tests/parity.py for the bound).
+e5m2: the block-scaled kernel with E5M2 operands, alone and paired with E4M3
+(kind::f8f6f4 takes the two formats independently).
+"""
+import pytest
+import torch
+
+import dense_gemm_blackwell_gb300 as dg
+from dense_gemm_blackwell_gb300 import inputs
+import oracle
+from parity import TOL_FP8, TOL_TF32, compare, dump_on_failure
+
+pytestmark = pytest.mark.gpu
+
+TDT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+CODE = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32, "tf32": dg.GEMM_TF32,
+        "e4m3": dg.GEMM_E4M3, "e5m2": dg.GEMM_E5M2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dg.build()
+    torch.cuda.init()
+
+
+def run(prob, out, **kw):
+    wl = prob.wl
+    db = wl.extra["dtype_b"]
+    A, B = prob.A.cuda(), prob.B.cuda()
+    sa = prob.scale_a.cuda() if prob.scale_a is not None else None
+    sb = prob.scale_b.cuda() if prob.scale_b is not None else None
+    D = torch.full((wl.M, wl.N), float("nan"), dtype=TDT[out], device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=CODE[wl.dtype_in], dtype_b=CODE[db], dtype_d=CODE[out],
+                        scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128 if sa is not None else 0, **kw)
+    with dg.Plan(desc) as plan:
+        plan.run(A, B, D, sa, sb)
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, (dg.gemm_status_string(s), rec.role)
+        info = plan.info.as_dict()
+    ref_a = "f32" if wl.dtype_in == "tf32" else wl.dtype_in
+    ref_b = "f32" if db == "tf32" else db
+    kw_o = {}
+    if sa is not None:
+        kw_o = dict(scale_a=prob.scale_a.numpy(), scale_b=prob.scale_b.numpy())
+    dref, s = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a=ref_a, dtype_b=ref_b, **kw_o)
+    return D.double().cpu().numpy(), dref[0], s[0], info
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_tf32_integers_bit_exact(cg_flag, out):
+    prob = inputs.make("square8192_bf16", M=600, N=712, K=1060, dist="ints", seed=71, dtype_in="tf32")
+    got, dref, s, info = run(prob, out, flags=cg_flag)
+    assert info["tile_k"] == 32
+    r = compare(got, dref, s, out, TOL_TF32, exact=True)
+    if not r["ok"]:
+        dump_on_failure("tf32_%s_%d" % (out, cg_flag), got=got, dref=dref, sabs=s)
+    assert r["ok"], r
+
+
+def test_tf32_random_and_stream_k():
+    prob = inputs.make("square4096_bf16", M=1024, N=1024, K=2048, seed=72, dtype_in="tf32")
+    got, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
+    assert info["stream_k_tiles"] > 0
+    r = compare(got, dref, s, "f32", TOL_TF32)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("fa,fb", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+def test_fp8_format_pairings_bit_exact(fa, fb):
+    prob = inputs.make("fp8_block8192", M=400, N=520, K=384, dist="ints", seed=73, dtype_in=fa, dtype_b=fb)
+    got, dref, s, info = run(prob, "bf16")
+    assert info["kernel"] == dg.GEMM_KERNEL_FP8_BLOCK
+    r = compare(got, dref, s, "bf16", TOL_FP8, exact=True)
+    assert r["ok"], r
+
+
+def test_e5m2_quantised_normal():
+    prob = inputs.make("fp8_block8192", M=300, N=520, K=512, seed=74, dtype_in="e5m2")
+    got, dref, s, info = run(prob, "bf16")
+    r = compare(got, dref, s, "bf16", TOL_FP8)
+    assert r["ok"], r

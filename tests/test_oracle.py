@@ -355,3 +355,35 @@ def test_zero_sized_and_k_zero():
     d, s = oracle.gemm(torch.zeros(3, 0, dtype=torch.float16), torch.zeros(4, 0, dtype=torch.float16),
                        M=3, N=4, K=0, dtype_a="f16", dtype_b="f16")
     assert (d == 0).all() and (s == 0).all()
+
+
+def test_decode_every_e5m2_code_matches_torch_and_ocp():
+    codes = np.arange(256, dtype=np.uint32)
+    mine = oracle.decode("e5m2", codes)
+    ref = torch.from_numpy(codes.astype(np.uint8)).view(torch.float8_e5m2).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    # OCP E5M2: IEEE-style infinities, largest finite 57344, smallest subnormal 2^-16
+    assert mine[0x7C] == np.inf and mine[0xFC] == -np.inf
+    assert mine[0x7B] == 57344.0 and mine[0x01] == 2.0 ** -16
+    assert oracle.encode("e5m2", [57344.0, 1.5])[:2].tolist() == [0x7B, 0x3E]
+
+
+def test_fp32_inputs_decode_exactly():
+    """32-bit input codes (tf32 products are checked against the exact fp32 values)."""
+    g = torch.Generator().manual_seed(61)
+    a = torch.randn(9, 40, generator=g)
+    b = torch.randn(7, 40, generator=g)
+    d, s = oracle.gemm(a.numpy(), b.numpy(), M=9, N=7, K=40, dtype_a="f32", dtype_b="f32")
+    rd, rs = _fsum_reference(a.double().numpy(), b.double().numpy())
+    assert (np.abs(d[0] - rd) <= 39 * 2.0 ** -53 * rs + np.spacing(np.abs(rd))).all()
+
+
+def test_mixed_fp8_formats():
+    g = torch.Generator().manual_seed(62)
+    qa = torch.randint(-3, 4, (6, 130), generator=g).float()
+    qb = torch.randint(-3, 4, (5, 130), generator=g).float()
+    d, _ = oracle.gemm(qa.to(torch.float8_e4m3fn), qb.to(torch.float8_e5m2), M=6, N=5, K=130,
+                       dtype_a="e4m3", dtype_b="e5m2")
+    assert np.array_equal(d[0], qa.double().numpy() @ qb.double().numpy().T)
