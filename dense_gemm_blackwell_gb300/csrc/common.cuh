@@ -39,6 +39,23 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t smem_addr) {
     return kSmemDescSw128KMajorBase | uint64_t((smem_addr >> 4) & 0x3FFFu);
 }
 
+// MN-major operand (M or N contiguous in memory) with the 128-byte swizzle:
+// each 128-byte row holds 64 consecutive M (or N) elements of one k, eight
+// k-rows form a 1024-byte atom.  The tile is stored as TMA boxes of 64
+// elements x 64 k-rows (8 KB), side by side along M/N.  Leading-dim offset =
+// 8 KB between 64-element atoms along M/N; stride-dim offset = 1024 B between
+// groups of 8 k-rows.  One K16 MMA spans 16 k-rows: +2048 B per MMA.
+constexpr uint32_t kMNMajorBoxBytes = 64 * 128;
+constexpr uint64_t kSmemDescSw128MNMajorBase =
+    (uint64_t(kMNMajorBoxBytes >> 4) << 16) |   // LBO: next 64 elements of M/N
+    (uint64_t(1024 >> 4) << 32) |                // SBO: next 8 k-rows
+    (uint64_t(1) << 46) |
+    (uint64_t(2) << 61);
+
+__host__ __device__ constexpr uint64_t smem_desc_sw128_mn(uint32_t smem_addr) {
+    return kSmemDescSw128MNMajorBase | uint64_t((smem_addr >> 4) & 0x3FFFu);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 / kind::f8f6f4 (public PTX ISA):
 //   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
 //   [15] A major (0 = K)       [16] B major      [17,23) N >> 3   [24,29) M >> 4
@@ -78,6 +95,8 @@ struct PersistentParams {
     int32_t batched;          // 1 = 3-D tensor maps
     int32_t tile_k;           // elements of K per ring stage (one 128-byte swizzle row)
     uint32_t mma_kind;        // kMmaKindF16 or kMmaKindTF32 (16-bit kernel only)
+    int32_t mn_major_a;       // 1: A is M-contiguous (loaded as 64x64 boxes, MN-major descriptor)
+    int32_t mn_major_b;       // 1: B is N-contiguous
     uint32_t idesc;
     uint32_t stage_bytes_a;   // per CTA
     uint32_t stage_bytes_b;   // per CTA

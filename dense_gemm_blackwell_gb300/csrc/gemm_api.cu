@@ -231,7 +231,10 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if (allow_single && single_fits(d)) return plan_single(d, props, info);
 
     // ------------------------------------------------ persistent pipelines
-    if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
+    // MN-major operands: 16-bit inputs only (tf32 needs K-major operands; the
+    // block-scaled kernel is K-major).
+    const bool mn_a = d.major_a == GEMM_MN_MAJOR, mn_b = d.major_b == GEMM_MN_MAJOR;
+    if ((mn_a || mn_b) && !is16(d.dtype_a)) return GEMM_ERR_UNSUPPORTED;
     if (is8(d.dtype_a)) return plan_fp8(d, props, info);
     const int out_bytes = elem_bytes(d.dtype_d);
     const int chunk_cols = 128 / out_bytes;
@@ -241,6 +244,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if (tile_n % 16 != 0 || tile_n < 16 || tile_n > 256) return GEMM_ERR_UNSUPPORTED;
     if (tile_n % chunk_cols != 0) return GEMM_ERR_UNSUPPORTED;     // epilogue writes 128-byte column chunks
     if ((tile_n / cg) % 8 != 0) return GEMM_ERR_UNSUPPORTED;      // B half-tile rows form 8-row swizzle atoms
+    if (mn_b && (tile_n / cg) % 64 != 0) return GEMM_ERR_UNSUPPORTED;  // MN-major B: 64-column boxes
     const int tmem_stages = 2;
     const int64_t tmem_need = tmem_stages * tile_n;
     if (tmem_need > 512) return GEMM_ERR_RESOURCES;
@@ -563,9 +567,17 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     // Tensor maps depend on the pointers only: re-encode when they change.
     if (!plan->maps_valid || plan->map_ptrs[0] != A || plan->map_ptrs[1] != B || plan->map_ptrs[2] != D) {
         plan->maps_valid = false;
-        if (!encode_map(&plan->maps[0], d.dtype_a, A, d.K, d.M, d.lda, batch_maps, d.stride_a, info.tile_k, 128) ||
-            !encode_map(&plan->maps[1], d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b, info.tile_k,
-                        info.tile_n / cg) ||
+        const bool mn_a = d.major_a == GEMM_MN_MAJOR, mn_b = d.major_b == GEMM_MN_MAJOR;
+        // K-major: (K, rows) boxes of tile_k x rows.  MN-major: (rows, K) boxes of 64 x tile_k.
+        const bool ok_a = mn_a ? encode_map(&plan->maps[0], d.dtype_a, A, d.M, d.K, d.lda, batch_maps, d.stride_a,
+                                            64, info.tile_k)
+                               : encode_map(&plan->maps[0], d.dtype_a, A, d.K, d.M, d.lda, batch_maps, d.stride_a,
+                                            info.tile_k, 128);
+        const bool ok_b = mn_b ? encode_map(&plan->maps[1], d.dtype_b, B, d.N, d.K, d.ldb, batch_maps, d.stride_b,
+                                            64, info.tile_k)
+                               : encode_map(&plan->maps[1], d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b,
+                                            info.tile_k, info.tile_n / cg);
+        if (!ok_a || !ok_b ||
             !encode_map(&plan->maps[2], d.dtype_d, D, d.N, d.M, d.ldd, batch_maps, d.stride_d, 128 / eb_d, 32)) {
             g_last_cuda_error = (int)cudaErrorInvalidValue;
             return GEMM_ERR_CUDA;
@@ -594,8 +606,11 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.tile_k = info.tile_k;
     p.mma_kind = d.dtype_a == GEMM_TF32 ? dgb::kMmaKindTF32 : dgb::kMmaKindF16;
     // A/B formats: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = tf32
+    p.mn_major_a = d.major_a == GEMM_MN_MAJOR;
+    p.mn_major_b = d.major_b == GEMM_MN_MAJOR;
     p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u),
-                              (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+                              (uint32_t)info.tile_m, (uint32_t)info.tile_n, (uint32_t)p.mn_major_a,
+                              (uint32_t)p.mn_major_b);
     p.stage_bytes_a = (uint32_t)(128 * info.tile_k * eb_a);
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
     p.flags = d.flags;

@@ -145,9 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                    const uint64_t da = smem_desc_sw128(sa);
-                    const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
-                    // four MMAs per 128-byte row: K16 of 16-bit elements or K8 of tf32
+                    const uint32_t sb = sa + p.stage_bytes_a;
+                    // K-major: next MMA's K is 32 bytes along the row (+2 in the
+                    // descriptor's address field); MN-major: 16 k-rows on (+128).
+                    const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+                    const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn(sb) : smem_desc_sw128(sb);
+                    const uint64_t step_a = p.mn_major_a ? 128u : 2u;
+                    const uint64_t step_b = p.mn_major_b ? 128u : 2u;
+                    // four MMAs per stage: K16 of 16-bit elements or K8 of tf32
                     if (p.mma_kind == kMmaKindTF32) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
@@ -155,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_f16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
+                            mma_f16<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc,
+                                        (kb != u.kb0) || (kk != 0));
                     }
                     issued_any = true;
                     commit_to<CG>(empty(stage));

@@ -123,6 +123,38 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Copy one operand's slice for one ring stage: `rows` rows (M or N) of
+// `tile_k` K elements.  K-major: one box of tile_k x rows.  MN-major: boxes of
+// 64 contiguous M/N elements x tile_k k-rows, one per 64 rows, 8 KB apart.
+template <int CG>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn_major,
+                                             int rows, int row0, int kx, int b, bool batched, bool hint,
+                                             uint64_t policy) {
+    const int boxes = mn_major ? rows / 64 : 1;
+    for (int j = 0; j < boxes; ++j) {
+        const int x = mn_major ? row0 + 64 * j : kx;
+        const int y = mn_major ? kx : row0;
+        const uint32_t d = dst + (uint32_t)j * kMNMajorBoxBytes;
+        if constexpr (CG == 1) {
+            if (batched) {
+                if (hint) tma_load_3d_hint(d, map, bar, x, y, b, policy);
+                else tma_load_3d(d, map, bar, x, y, b);
+            } else {
+                if (hint) tma_load_2d_hint(d, map, bar, x, y, policy);
+                else tma_load_2d(d, map, bar, x, y);
+            }
+        } else {
+            if (batched) {
+                if (hint) tma_load_3d_pair_hint(d, map, bar, x, y, b, policy);
+                else tma_load_3d_pair(d, map, bar, x, y, b);
+            } else {
+                if (hint) tma_load_2d_pair_hint(d, map, bar, x, y, policy);
+                else tma_load_2d_pair(d, map, bar, x, y);
+            }
+        }
+    }
+}
+
 // TMA producer (one thread).  `tile_k` is the ring stage depth in elements of
 // A/B (one 128-byte swizzle row: 64 for 16-bit, 128 for 8-bit types).
 template <int CG>
@@ -162,27 +194,10 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                 const uint32_t sb = sa + p.stage_bytes_a;
                 const int kx = kb * tile_k;
-                if constexpr (CG == 1) {
-                    if (p.batched) {
-                        if (keep_a) tma_load_3d_hint(sa, &p.tmap_a, fb, kx, a_row, b, pol_a);
-                        else tma_load_3d(sa, &p.tmap_a, fb, kx, a_row, b);
-                        tma_load_3d(sb, &p.tmap_b, fb, kx, b_row, b);
-                    } else {
-                        if (keep_a) tma_load_2d_hint(sa, &p.tmap_a, fb, kx, a_row, pol_a);
-                        else tma_load_2d(sa, &p.tmap_a, fb, kx, a_row);
-                        tma_load_2d(sb, &p.tmap_b, fb, kx, b_row);
-                    }
-                } else {
-                    if (p.batched) {
-                        if (keep_a) tma_load_3d_pair_hint(sa, &p.tmap_a, fb, kx, a_row, b, pol_a);
-                        else tma_load_3d_pair(sa, &p.tmap_a, fb, kx, a_row, b);
-                        tma_load_3d_pair(sb, &p.tmap_b, fb, kx, b_row, b);
-                    } else {
-                        if (keep_a) tma_load_2d_pair_hint(sa, &p.tmap_a, fb, kx, a_row, pol_a);
-                        else tma_load_2d_pair(sa, &p.tmap_a, fb, kx, a_row);
-                        tma_load_2d_pair(sb, &p.tmap_b, fb, kx, b_row);
-                    }
-                }
+                load_operand<CG>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0, keep_a,
+                                 pol_a);
+                load_operand<CG>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b, p.batched != 0, false,
+                                 pol_a);
             }
             ++issued;
             if (++stage == S) { stage = 0; phase ^= 1u; }

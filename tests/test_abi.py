@@ -122,10 +122,21 @@ def test_degenerate_sizes_plan():
     assert s == dg.GEMM_OK and info.kernel == 0
 
 
-def test_mn_major_only_on_single_cta():
+def test_mn_major_plans():
     s, info = query(M=100, N=72, K=40, major_a=dg.GEMM_MN_MAJOR, major_b=dg.GEMM_MN_MAJOR)
     assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_SINGLE_CTA
-    s, _ = query(M=1000, N=72, K=40, major_b=dg.GEMM_MN_MAJOR)
+    s, info = query(M=1000, N=72, K=40, major_b=dg.GEMM_MN_MAJOR)
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT
+    s, info = query(M=8192, N=8192, K=8192, major_a=dg.GEMM_MN_MAJOR, major_b=dg.GEMM_MN_MAJOR)
+    assert s == dg.GEMM_OK and info.cta_group == 2
+    # MN-major B is loaded in 64-column boxes: a pair's half tile must be a multiple of 64
+    s, _ = query(M=8192, N=8192, K=8192, major_b=dg.GEMM_MN_MAJOR, flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=192)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
+    # tf32 needs K-major operands; the block-scaled kernel is K-major
+    s, _ = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, major_a=dg.GEMM_MN_MAJOR)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
+    s, _ = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, major_b=dg.GEMM_MN_MAJOR,
+                 scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
     assert s == dg.GEMM_ERR_UNSUPPORTED
 
 
