@@ -145,6 +145,8 @@ bool single_fits(const gemm_desc_t& d) {
 // block of B's scales), 128-deep K stages, two TMEM partial buffers of 256
 // columns, 8 promotion/epilogue warps with one 4 KB staging buffer each.
 constexpr int kFp8Threads = 320;
+constexpr int kFp8DefaultTileN = 256;           // planner default for block-scaled problems
+constexpr int kFp8DefaultCtaGroupNarrow = 2;    // pair form for 128-wide tiles
 constexpr int64_t kFp8StagingBytes = 8 * 32 * 128;
 
 int choose_cta_group(const gemm_desc_t& d, const gemm_device_props_t& props, int64_t tile_n) {
@@ -158,15 +160,28 @@ int choose_cta_group(const gemm_desc_t& d, const gemm_device_props_t& props, int
 }
 
 gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
-    if (d.tile_n != 0 && d.tile_n != 256) return GEMM_ERR_UNSUPPORTED;
-    const int64_t tile_n = 256;
-    // The promotion couples the pair's two epilogues per K block; single-SM
-    // tiles measured 2.2x faster on GB300, so the pair form is opt-in.
-    const int cg = (d.flags & GEMM_FLAG_CTA_GROUP_2) ? 2 : 1;
+    // Tiles 256 or 128 columns wide (each promotion warp owns half of them, one
+    // 128-column block of B's scales at most); 512 / tile_n TMEM partials.
+    if (d.tile_n != 0 && d.tile_n != 256 && d.tile_n != 128) return GEMM_ERR_UNSUPPORTED;
+    int cg;
+    int64_t tile_n;
+    if (d.flags & GEMM_FLAG_CTA_GROUP_1) {
+        cg = 1;
+        tile_n = d.tile_n ? d.tile_n : 256;
+    } else if (d.flags & GEMM_FLAG_CTA_GROUP_2) {
+        cg = 2;
+        tile_n = d.tile_n ? d.tile_n : 128;
+    } else {
+        tile_n = d.tile_n ? d.tile_n : kFp8DefaultTileN;
+        cg = tile_n == 128 ? kFp8DefaultCtaGroupNarrow : 1;
+        if (cg == 2 && !(d.M > 128 && ceil_div(d.M, 256) * ceil_div(d.N, tile_n) * d.batch >= props.sm_count / 2))
+            cg = 1;
+    }
     const int tile_k = 128;
+    const int partials = (int)(512 / tile_n);
     const int64_t stage_bytes = 128 * tile_k + (tile_n / cg) * tile_k;
     auto smem_for = [&](int64_t s) {
-        return s * stage_bytes + kFp8StagingBytes + 8 * (2 * s + 4 + 1) + 8 + kAlignSlack;
+        return s * stage_bytes + kFp8StagingBytes + 8 * (2 * s + 2 * 4 + 1) + 8 + kAlignSlack;
     };
     int64_t stages = d.stages;
     if (stages == 0) {
@@ -186,13 +201,13 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
     info->tile_n = (int32_t)tile_n;
     info->tile_k = tile_k;
     info->stages = (int32_t)stages;
-    info->tmem_stages = 2;
+    info->tmem_stages = partials;
     info->tmem_cols = 512;
     info->grid = (int32_t)(clusters * cg);
     info->block_threads = kFp8Threads;
     info->num_tiles = tiles;
     info->stage_bytes = stage_bytes;
-    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * 2) + 4;
+    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * partials) + 4;
     info->smem_bytes = smem_for(stages);
     return GEMM_OK;
 }
@@ -381,7 +396,7 @@ gemm_status_t cap_resident(const gemm_desc_t& d, gemm_plan_info_t* info) {
     if (info->kernel == GEMM_KERNEL_PERSISTENT)
         resident = dgb::persistent_max_active_clusters(info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
     else if (info->kernel == GEMM_KERNEL_FP8_BLOCK)
-        resident = dgb::fp8_max_active_clusters(info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
+        resident = dgb::fp8_max_active_clusters(info->cta_group, info->tile_n, d.dtype_d, (size_t)info->smem_bytes);
     else
         return GEMM_OK;
     if (resident <= 0) return cuda_fail(cudaGetLastError());

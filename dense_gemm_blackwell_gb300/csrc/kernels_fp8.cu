@@ -39,12 +39,17 @@ constexpr int kFp8TileK = 128;              // e4m3 elements per ring stage (128
 constexpr int kFp8EpiWarps = 8;
 constexpr int kFp8Threads = 64 + 32 * kFp8EpiWarps;
 constexpr uint32_t kFp8StagingBytes = 32 * 128;   // one buffer per epilogue warp
+constexpr int kFp8MaxPartials = 4;                 // partial buffers: 512 TMEM columns / tile_n
 
-template <int CG, int OUT>
+// COLS: columns of the tile each promotion warp owns (tile_n / 2): 128 for
+// 256-wide tiles, 64 for 128-wide tiles.  The tile has 512 / tile_n partial
+// buffers in TMEM (2 or 4), so the MMA can run that many blocks minus one
+// ahead of the promotion.
+template <int CG, int OUT, int COLS>
 __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_constant__ PersistentParams p) {
     constexpr int kOutBytes = (OUT == GEMM_F32) ? 4 : 2;
     constexpr int kChunkCols = 128 / kOutBytes;          // columns per 128-byte staging row
-    constexpr int kChunks = 128 / kChunkCols;            // chunks per warp's 128 columns
+    constexpr int kChunks = COLS / kChunkCols;           // chunks per warp's columns
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -54,14 +59,15 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kFp8EpiWarps * kFp8StagingBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4 + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * kFp8MaxPartials + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8u * S;
-    const uint32_t pfull0 = empty0 + 8u * S;     // partial buffer written (2)
-    const uint32_t pempty0 = pfull0 + 16u;       // partial buffer read (2)
-    const uint32_t drain_bar = pempty0 + 16u;
+    const int PB = p.tmem_stages;                // partial buffers (2 or 4)
+    const uint32_t pfull0 = empty0 + 8u * S;     // partial buffer written
+    const uint32_t pempty0 = pfull0 + 8u * kFp8MaxPartials;   // partial buffer read
+    const uint32_t drain_bar = pempty0 + 8u * kFp8MaxPartials;
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
         }
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < PB; ++j) {
             mbar_init(pfull0 + 8u * j, 1);
             mbar_init(pempty0 + 8u * j, CG * kFp8EpiWarps);
         }
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                     commit_to<CG>(empty0 + 8u * stage);
                     commit_to<CG>(pfull0 + 8u * pb);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
-                    if (++pb == 2) { pb = 0; pphase ^= 1u; }
+                    if (++pb == PB) { pb = 0; pphase ^= 1u; }
                 }
             }
             if (aborted && issued_any) {
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
         const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
         const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                  // TMEM lane quarter
-        const int half = (warp - 2) >> 2;         // which 128 columns of the tile
+        const int half = (warp - 2) >> 2;         // which COLS columns of the tile
         uint8_t* buf = staging + (warp - 2) * kFp8StagingBytes;
         int pb = 0;
         uint32_t pphase = 0;
@@ -164,14 +170,14 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             tile_coords(p, t, b, mb, nb);
             const int m_warp = mb * (128 * CG) + (int)rank * 128 + wq * 32;
             const int row = m_warp + lane;
-            const int col0 = nb * p.tile_n + half * 128;
+            const int col0 = nb * p.tile_n + half * COLS;   // inside one 128-column block of B's scales
             const bool row_ok = row < p.M;
             const bool cols_ok = col0 < p.N;
             const float* sa_row = p.scale_a + (size_t)b * p.stride_sa + (size_t)(row_ok ? row : 0) * p.ld_sa;
             const float* sb_blk = p.scale_b + (size_t)b * p.stride_sb + (size_t)(cols_ok ? col0 / 128 : 0) * p.ld_sb;
-            float acc[128];
+            float acc[COLS];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
             // Scales are loaded two blocks ahead so that their L2 latency hides
             // behind the promotion of the blocks in between.
             const bool scaled = row_ok && cols_ok;
@@ -192,23 +198,45 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 if (!ok) { aborted = true; break; }
                 tc_fence_after();
                 if (cols_ok) {
-                    const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(pb * p.tile_n + half * 128);
-                    // 16-column loads keep the register footprint within what a
-                    // 10-warp CTA can hold (3 warps share a sub-partition's 16K registers).
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(taddr + c * 16, r);
+                    const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(pb * p.tile_n + half * COLS);
+                    if constexpr (COLS == 64) {
+                        // all four 16-column loads in flight, one wait
+                        uint32_t r0[16], r1[16], r2[16], r3[16];
+                        tmem_ld_32x32b_x16(taddr, r0);
+                        tmem_ld_32x32b_x16(taddr + 16, r1);
+                        tmem_ld_32x32b_x16(taddr + 32, r2);
+                        tmem_ld_32x32b_x16(taddr + 48, r3);
                         tmem_wait_ld();
-                        tmem_reg_fence16(r);
+                        tmem_reg_fence16(r0);
+                        tmem_reg_fence16(r1);
+                        tmem_reg_fence16(r2);
+                        tmem_reg_fence16(r3);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 16 + i]);
+                        for (int i = 0; i < 16; ++i) {
+                            acc[i] = fmaf(__uint_as_float(r0[i]), s, acc[i]);
+                            acc[16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[16 + i]);
+                            acc[32 + i] = fmaf(__uint_as_float(r2[i]), s, acc[32 + i]);
+                            acc[48 + i] = fmaf(__uint_as_float(r3[i]), s, acc[48 + i]);
+                        }
+                    } else {
+                        // 16-column loads keep the register footprint within what a
+                        // 10-warp CTA can hold (3 warps share a sub-partition's 16K registers).
+#pragma unroll
+                        for (int c = 0; c < COLS / 16; ++c) {
+                            uint32_t r[16];
+                            tmem_ld_32x32b_x16(taddr + c * 16, r);
+                            tmem_wait_ld();
+                            tmem_reg_fence16(r);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 16 + i]);
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive_leader<CG>(pempty0 + 8u * pb);
-                if (++pb == 2) { pb = 0; pphase ^= 1u; }
+                if (++pb == PB) { pb = 0; pphase ^= 1u; }
             }
             if (aborted || !cols_ok || m_warp >= p.M) continue;
 #pragma unroll
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     }
 }
 
-template <int CG, int OUT>
+template <int CG>
 static cudaLaunchConfig_t fp8_config(size_t smem, int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -275,53 +303,50 @@ static cudaLaunchConfig_t fp8_config(size_t smem, int grid, cudaStream_t stream,
     return cfg;
 }
 
-template <int CG, int OUT>
+template <int CG, int OUT, int COLS>
 static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = fp8_block_kernel<CG, OUT>;
+    auto kern = fp8_block_kernel<CG, OUT, COLS>;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, grid, stream, attr);
+    cudaLaunchConfig_t cfg = fp8_config<CG>(smem, grid, stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int CG, int OUT>
+template <int CG, int OUT, int COLS>
 static int fp8_clusters_typed(size_t smem) {
-    auto kern = fp8_block_kernel<CG, OUT>;
+    auto kern = fp8_block_kernel<CG, OUT, COLS>;
     static std::atomic<int> smem_set[kMaxDevices];
     if (ensure_smem_limit(kern, smem, smem_set) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = fp8_config<CG, OUT>(smem, CG, nullptr, attr);
+    cudaLaunchConfig_t cfg = fp8_config<CG>(smem, CG, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
     return n;
 }
 
-#define DGB_FP8_DISPATCH(FN, ...)                                                        \
-    if (cta_group == 1) {                                                                \
-        switch (dtype_d) {                                                               \
-        case GEMM_F32: return FN<1, GEMM_F32>(__VA_ARGS__);                              \
-        case GEMM_BF16: return FN<1, GEMM_BF16>(__VA_ARGS__);                            \
-        case GEMM_F16: return FN<1, GEMM_F16>(__VA_ARGS__);                              \
-        default: break;                                                                  \
-        }                                                                                \
-    } else {                                                                             \
-        switch (dtype_d) {                                                               \
-        case GEMM_F32: return FN<2, GEMM_F32>(__VA_ARGS__);                              \
-        case GEMM_BF16: return FN<2, GEMM_BF16>(__VA_ARGS__);                            \
-        case GEMM_F16: return FN<2, GEMM_F16>(__VA_ARGS__);                              \
-        default: break;                                                                  \
-        }                                                                                \
+#define DGB_FP8_DISPATCH_OUT(FN, CGV, COLSV, ...)                                        \
+    switch (dtype_d) {                                                                   \
+    case GEMM_F32: return FN<CGV, GEMM_F32, COLSV>(__VA_ARGS__);                         \
+    case GEMM_BF16: return FN<CGV, GEMM_BF16, COLSV>(__VA_ARGS__);                       \
+    case GEMM_F16: return FN<CGV, GEMM_F16, COLSV>(__VA_ARGS__);                         \
+    default: break;                                                                      \
     }
+#define DGB_FP8_DISPATCH(FN, ...)                                                        \
+    if (cta_group == 1 && tile_n == 256) { DGB_FP8_DISPATCH_OUT(FN, 1, 128, __VA_ARGS__) } \
+    if (cta_group == 1 && tile_n == 128) { DGB_FP8_DISPATCH_OUT(FN, 1, 64, __VA_ARGS__) }  \
+    if (cta_group == 2 && tile_n == 256) { DGB_FP8_DISPATCH_OUT(FN, 2, 128, __VA_ARGS__) } \
+    if (cta_group == 2 && tile_n == 128) { DGB_FP8_DISPATCH_OUT(FN, 2, 64, __VA_ARGS__) }
 
 cudaError_t launch_fp8_block(const PersistentParams& p, int cta_group, int dtype_d, int grid, size_t smem_bytes,
                              cudaStream_t stream) {
+    const int tile_n = p.tile_n;
     DGB_FP8_DISPATCH(fp8_launch_typed, p, grid, smem_bytes, stream)
     return cudaErrorInvalidValue;
 }
 
-int fp8_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes) {
+int fp8_max_active_clusters(int cta_group, int tile_n, int dtype_d, size_t smem_bytes) {
     DGB_FP8_DISPATCH(fp8_clusters_typed, smem_bytes)
     return 0;
 }

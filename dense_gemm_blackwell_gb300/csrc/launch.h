@@ -22,7 +22,7 @@ int persistent_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes
 // Block-scaled e4m3 kernel: grid = CTAs (a multiple of cta_group), block = 320 threads.
 cudaError_t launch_fp8_block(const PersistentParams& p, int cta_group, int dtype_d, int grid, size_t smem_bytes,
                              cudaStream_t stream);
-int fp8_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes);
+int fp8_max_active_clusters(int cta_group, int tile_n, int dtype_d, size_t smem_bytes);
 
 // Zero fill of D (K == 0).
 cudaError_t launch_zero_fill(void* D, int dtype_d, int64_t M, int64_t N, int64_t batch, int64_t ldd,

@@ -165,8 +165,12 @@ def test_fp8_block_plan():
     # e4m3 requires block scales; 16-bit inputs refuse them
     s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3)
     assert s == dg.GEMM_ERR_UNSUPPORTED
+    # tiles are 128 or 256 wide (4 or 2 TMEM partials); other widths are refused
+    s, info = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128,
+                    tile_n=128)
+    assert s == dg.GEMM_OK and info.tmem_stages == 4
     s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128,
-                 tile_n=128)
+                 tile_n=192)
     assert s == dg.GEMM_ERR_UNSUPPORTED
 
 

@@ -50,11 +50,15 @@ def oracle_fp8(prob, rows=None):
                             scale_a=prob.scale_a.numpy(), scale_b=prob.scale_b.numpy(), rows=rows)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
 @pytest.mark.parametrize("out", ["bf16", "f32", "f16"])
-def test_fp8_integers_bit_exact(cg_flag, out):
+def test_fp8_integers_bit_exact(cg_flag, out, tile_n):
+    """Both tile widths (2 or 4 TMEM partial buffers, 128 or 64 columns per
+    promotion warp) on both CTA groups."""
     prob = inputs.make("fp8_block8192", M=520, N=600, K=400, dist="ints", seed=31)
-    D, info = run_fp8(prob, out, flags=cg_flag)
+    D, info = run_fp8(prob, out, flags=cg_flag, tile_n=tile_n)
+    assert info["tile_n"] == tile_n and info["tmem_stages"] == 512 // tile_n
     dref, s = oracle_fp8(prob)
     got = D.double().cpu().numpy()
     r = compare(got, dref[0], s[0], out, TOL_FP8, exact=True)
@@ -63,10 +67,11 @@ def test_fp8_integers_bit_exact(cg_flag, out):
     assert r["ok"], (r, info)
 
 
-@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
-def test_fp8_quantised_normal(cg_flag):
+@pytest.mark.parametrize("cg_flag,tile_n", [(dg.GEMM_FLAG_CTA_GROUP_1, 256), (dg.GEMM_FLAG_CTA_GROUP_2, 128),
+                                            (dg.GEMM_FLAG_CTA_GROUP_2, 256), (dg.GEMM_FLAG_CTA_GROUP_1, 128)])
+def test_fp8_quantised_normal(cg_flag, tile_n):
     prob = inputs.make("fp8_block8192", M=300, N=520, K=512, seed=32)
-    D, info = run_fp8(prob, "bf16", flags=cg_flag)
+    D, info = run_fp8(prob, "bf16", flags=cg_flag, tile_n=tile_n)
     dref, s = oracle_fp8(prob)
     r = compare(D.double().cpu().numpy(), dref[0], s[0], "bf16", TOL_FP8)
     assert r["ok"], (r, info)
