@@ -181,20 +181,25 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
     const int partials = (int)(512 / tile_n);
     const int64_t stage_bytes = 128 * tile_k + (tile_n / cg) * tile_k;
     auto smem_for = [&](int64_t s) {
-        return s * stage_bytes + kFp8StagingBytes + 8 * (2 * s + 2 * 4 + 1) + 8 + kAlignSlack;
+        return s * stage_bytes + kFp8StagingBytes + 8 * (2 * s + 1) + 8 + kAlignSlack;
     };
     int64_t stages = d.stages;
     if (stages == 0) {
         stages = 16;
         while (stages > 2 && smem_for(stages) > props.smem_optin_bytes) --stages;
     }
-    if (stages < 2 || stages > 16) return GEMM_ERR_UNSUPPORTED;
+    // the promotion warps track a block's MMAs through its stage's empty barrier
+    // and release partials onto full barriers PB blocks ahead: both stay within
+    // one phase of their users only if stages >= partials
+    if (stages < 2 || stages > 16 || stages < partials) return GEMM_ERR_UNSUPPORTED;
     if (smem_for(stages) > props.smem_optin_bytes) return GEMM_ERR_RESOURCES;
     const int64_t tiles = ceil_div(d.M, 128 * cg) * ceil_div(d.N, tile_n) * d.batch;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     int64_t clusters = props.sm_count / cg;
     if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
     clusters = std::min<int64_t>(clusters, tiles);
+    // the promotion warps count a CTA's K blocks over all its tiles in an int
+    if (ceil_div(tiles, clusters) * ceil_div(d.K, tile_k) > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     info->kernel = GEMM_KERNEL_FP8_BLOCK;
     info->cta_group = cg;
     info->tile_m = 128 * cg;
@@ -207,7 +212,7 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
     info->block_threads = kFp8Threads;
     info->num_tiles = tiles;
     info->stage_bytes = stage_bytes;
-    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages + 2 * partials) + 4;
+    info->pipeline_bytes = stages * stage_bytes + 8 * (2 * stages) + 4;
     info->smem_bytes = smem_for(stages);
     return GEMM_OK;
 }

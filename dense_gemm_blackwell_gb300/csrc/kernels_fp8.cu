@@ -12,8 +12,8 @@
 //                      stage (one 128-byte swizzle row of e4m3).
 //   warp 1           : allocates tensor memory; one lane of the pair leader
 //                      issues four K32 tcgen05.mma kind::f8f6f4 per block into a
-//                      fresh partial P[j mod 2] (j counts blocks over all tiles)
-//                      and commits it to the partial's full barrier.
+//                      fresh partial P[j mod PB] (j counts blocks over all tiles)
+//                      and commits them to the stage's empty barrier.
 //   warps 2..9       : promotion and epilogue.  Warp w owns TMEM lanes
 //                      32*(w mod 4).. (its 32 rows) and 128 of the tile's 256
 //                      columns (half (w-2)/4, exactly one 128-row block of B).
@@ -23,8 +23,20 @@
 //                      After the tile's last block: convert, stage in swizzled
 //                      shared memory, TMA store.
 //
-// Two partial buffers let the tensor core compute block j+1 while the
+// Two or four partial buffers let the tensor core compute block j+1 while the
 // epilogue warps promote block j.  Waits are bounded as in the 16-bit kernel.
+//
+// One barrier wait per block in the MMA thread.  In a thread with tcgen05.mma
+// in flight every mbarrier probe costs about 230 cycles (22 in a thread
+// without; measured on GB300), and four K32 MMAs of a 128 x 256 block take
+// 512 cycles, so the MMA thread cannot afford to wait for both the stage's
+// data and the partial's release.  Block j's full barrier therefore carries
+// both: the producer's arrival with the expected bytes, plus one arrival from
+// every promotion warp of the pair once it has read partial j mod PB back for
+// block j - PB (the first PB blocks get theirs up front).  The promotion warps
+// learn that a block's MMAs completed from the stage's empty barrier (the
+// MMA's single commit per block).  With the ring at least as deep as the
+// partial count, neither barrier can run a phase ahead of the warps that use it.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,7 +51,6 @@ constexpr int kFp8TileK = 128;              // e4m3 elements per ring stage (128
 constexpr int kFp8EpiWarps = 8;
 constexpr int kFp8Threads = 64 + 32 * kFp8EpiWarps;
 constexpr uint32_t kFp8StagingBytes = 32 * 128;   // one buffer per epilogue warp
-constexpr int kFp8MaxPartials = 4;                 // partial buffers: 512 TMEM columns / tile_n
 
 // COLS: columns of the tile each promotion warp owns (tile_n / 2): 128 for
 // 256-wide tiles, 64 for 128-wide tiles.  The tile has 512 / tile_n partial
@@ -59,15 +70,13 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kFp8EpiWarps * kFp8StagingBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * kFp8MaxPartials + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8u * S;
-    const int PB = p.tmem_stages;                // partial buffers (2 or 4)
-    const uint32_t pfull0 = empty0 + 8u * S;     // partial buffer written
-    const uint32_t pempty0 = pfull0 + 8u * kFp8MaxPartials;   // partial buffer read
-    const uint32_t drain_bar = pempty0 + 8u * kFp8MaxPartials;
+    const int PB = p.tmem_stages;                // partial buffers (2 or 4), PB <= S
+    const uint32_t drain_bar = empty0 + 8u * S;
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
@@ -76,12 +85,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8u * s, 1);
+            mbar_init(full0 + 8u * s, 1 + CG * kFp8EpiWarps);   // producer + partial released
             mbar_init(empty0 + 8u * s, 1);
-        }
-        for (int j = 0; j < PB; ++j) {
-            mbar_init(pfull0 + 8u * j, 1);
-            mbar_init(pempty0 + 8u * j, CG * kFp8EpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -117,17 +122,11 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             int stage = 0;
             uint32_t phase = 0;
             int pb = 0;
-            uint32_t pphase = 0;
             bool aborted = false;
             bool issued_any = false;
             for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!wait_phase<CG == 2>(pempty0 + 8u * pb, pphase ^ 1u, abort_flag, tmo, p.status, kRoleMma,
-                                             pb, t)) {
-                        aborted = true;
-                        break;
-                    }
-                    tc_fence_after();
+                    // completes once the block's bytes landed and its partial is free
                     if (!wait_phase<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma, stage,
                                            t)) {
                         aborted = true;
@@ -142,10 +141,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                     for (int kk = 0; kk < kFp8TileK / 32; ++kk)
                         mma_f8<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, kk != 0);
                     issued_any = true;
-                    commit_to<CG>(empty0 + 8u * stage);
-                    commit_to<CG>(pfull0 + 8u * pb);
+                    commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
                     if (++stage == S) { stage = 0; phase ^= 1u; }
-                    if (++pb == PB) { pb = 0; pphase ^= 1u; }
+                    if (++pb == PB) pb = 0;
                 }
             }
             if (aborted && issued_any) {
@@ -163,8 +161,16 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
         const int half = (warp - 2) >> 2;         // which COLS columns of the tile
         uint8_t* buf = staging + (warp - 2) * kFp8StagingBytes;
         int pb = 0;
-        uint32_t pphase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool aborted = false;
+        // blocks this CTA has still to promote, over all its tiles (the plan
+        // keeps the count within int)
+        const int my_tiles = cluster_id < p.num_tiles ? (p.num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
+        int left = my_tiles * p.num_k_blocks;
+        // the first PB blocks find their partials free
+        if (lane == 0)
+            for (int i = 0; i < PB && i < left; ++i) arrive_leader<CG>(full0 + 8u * i);
         for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
             int b, mb, nb;
             tile_coords(p, t, b, mb, nb);
@@ -193,7 +199,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 sb1 = (scaled && kb + 2 < nkb) ? __ldg(sb_blk + kb + 2) : 0.0f;
                 int ok = 0;
                 if (lane == 0)
-                    ok = wait_phase<false>(pfull0 + 8u * pb, pphase, abort_flag, tmo, p.status, kRoleEpilogue, pb, t);
+                    ok = wait_phase<false>(empty0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleEpilogue,
+                                           stage, t);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { aborted = true; break; }
                 tc_fence_after();
@@ -235,8 +242,14 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_leader<CG>(pempty0 + 8u * pb);
-                if (++pb == PB) { pb = 0; pphase ^= 1u; }
+                // partial pb is free again: count towards block j + PB's full barrier
+                if (lane == 0 && left > PB) {
+                    const int rs = stage + PB < S ? stage + PB : stage + PB - S;
+                    arrive_leader<CG>(full0 + 8u * rs);
+                }
+                --left;
+                if (++pb == PB) pb = 0;
+                if (++stage == S) { stage = 0; phase ^= 1u; }
             }
             if (aborted || !cols_ok || m_warp >= p.M) continue;
 #pragma unroll
@@ -275,6 +288,18 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 }
             }
         }
+        // Abort while waiting for block j (at `stage`, `left` blocks to go):
+        // give this warp's arrival to the blocks it has not released yet that
+        // the ring can hold, j + PB .. j + S - 1, so that a stage whose copies
+        // are in flight still completes and the producer's drain sees them
+        // land.  Their previous phases (blocks < j) are complete, and the warp
+        // arrives at most once per phase: no barrier is over-arrived (a phase
+        // still waiting for bytes must get no arrival beyond its count).
+        if (aborted && lane == 0)
+            for (int x = PB; x < S && x < left; ++x) {
+                const int rs = stage + x < S ? stage + x : stage + x - S;
+                arrive_leader<CG>(full0 + 8u * rs);
+            }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }

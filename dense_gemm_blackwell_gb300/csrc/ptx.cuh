@@ -76,8 +76,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Arrive on a barrier of another CTA of the cluster (address from map_to_cta).
+// Default semantics (release at CTA scope): every use hands back tensor memory
+// whose tcgen05.ld reads were already waited for, so no cluster-scope release
+// of the thread's other memory accesses is needed -- and a cluster-scope
+// release would stall until the thread's outstanding global loads complete
+// (measured: about 1,300 cycles per hand-back in the block-scaled kernel).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];"
                  :: "r"(cluster_addr) : "memory");
 }
 

@@ -17,6 +17,7 @@ import torch
 import dense_gemm_blackwell_gb300 as dg
 from dense_gemm_blackwell_gb300 import inputs
 import oracle
+from parity import TOL_FP8, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -54,3 +55,34 @@ def test_dropped_copy_times_out_and_context_survives(cg_flag, ctas):
         assert plan.sync_status()[0] == dg.GEMM_OK
     dref, _ = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="bf16", dtype_b="bf16")
     assert np.array_equal(D.double().cpu().numpy(), dref[0])
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+def test_fp8_dropped_copy_times_out_and_context_survives(cg_flag):
+    """Same for the block-scaled kernel, whose full barriers also count the
+    promotion warps' partial releases: the abort path must still drain."""
+    prob = inputs.make("fp8_block8192", M=1024, N=1024, K=1024, seed=43)
+    wl = prob.wl
+    A, B = prob.A.cuda(), prob.B.cuda()
+    SA, SB = prob.scale_a.cuda(), prob.scale_b.cuda()
+    D = torch.zeros(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    common = dict(dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_BF16, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    desc = dg.make_desc(wl.M, wl.N, wl.K, flags=cg_flag | dg.GEMM_FLAG_TEST_DROP_LOAD,
+                        wait_timeout_ns=20_000_000, **common)
+    with dg.Plan(desc) as plan:
+        t0 = time.time()
+        plan.run(A, B, D, SA, SB)
+        status, rec = plan.sync_status()
+        elapsed = time.time() - t0
+        assert status == dg.GEMM_ERR_TIMEOUT
+        assert rec.code == dg.GEMM_ERR_TIMEOUT and rec.role in (1, 2, 3)
+        assert elapsed < 5.0
+        assert plan.sync_status()[0] == dg.GEMM_OK
+
+    desc_ok = dg.make_desc(wl.M, wl.N, wl.K, flags=cg_flag, **common)
+    with dg.Plan(desc_ok) as plan:
+        plan.run(A, B, D, SA, SB)
+        assert plan.sync_status()[0] == dg.GEMM_OK
+    dref, sabs = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="e4m3", dtype_b="e4m3",
+                             scale_a=prob.scale_a.numpy(), scale_b=prob.scale_b.numpy())
+    assert compare(D.double().cpu().numpy(), dref[0], sabs[0], "bf16", TOL_FP8)["ok"]
