@@ -93,7 +93,8 @@ struct PersistentParams {
     int32_t tile_n, stages, tmem_cols, tmem_stages;
     int32_t group_m;
     int32_t batched;          // 1 = 3-D tensor maps
-    int32_t tile_k;           // elements of K per ring stage (one 128-byte swizzle row)
+    int32_t tile_k;           // elements of K per ring stage (k_atoms 128-byte swizzle rows)
+    int32_t k_atoms;          // 128-byte K atoms per stage (1 or 2; 2 only with K-major operands)
     uint32_t mma_kind;        // kMmaKindF16 or kMmaKindTF32 (16-bit kernel only)
     int32_t mn_major_a;       // 1: A is M-contiguous (loaded as 64x64 boxes, MN-major descriptor)
     int32_t mn_major_b;       // 1: B is N-contiguous

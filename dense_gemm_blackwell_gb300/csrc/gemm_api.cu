@@ -270,9 +270,26 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if (tmem_need > 512) return GEMM_ERR_RESOURCES;
     const int tmem_cols = pow2_at_least(tmem_need);
 
-    const int tile_k = 128 / elem_bytes(d.dtype_a);  // one 128-byte swizzle row: 64 16-bit or 32 tf32 elements
-    const int64_t stage_a = 128 * 128;              // 128 rows x 128 B
-    const int64_t stage_b = (tile_n / cg) * 128;
+    // Ring stage depth: one or two 128-byte swizzle atoms of K (64 or 128
+    // 16-bit elements, 32 or 64 tf32).  Two atoms halve the MMA thread's
+    // barrier waits per MMA (its issue loop is the bottleneck at one atom:
+    // 8192^3 bf16 runs 5.9 % faster on GB300); default whenever both operands
+    // are K-major, K spans more than one atom and three stages still fit.
+    if ((d.flags & GEMM_FLAG_STAGE_K1) && (d.flags & GEMM_FLAG_STAGE_K2)) return GEMM_ERR_INVALID_ARG;
+    if ((d.flags & GEMM_FLAG_STAGE_K2) && (mn_a || mn_b)) return GEMM_ERR_UNSUPPORTED;
+    const int64_t atom_k = 128 / elem_bytes(d.dtype_a);
+    const int64_t atom_bytes = 128 * 128 + (tile_n / cg) * 128;   // A and B, one atom of K
+    const int64_t fixed_bytes = kStagingBytes + 8 * (2 * tmem_stages + 1) + 8 + kAlignSlack;
+    int atoms = 1;
+    if (d.flags & GEMM_FLAG_STAGE_K2) {
+        atoms = 2;
+    } else if (!(d.flags & GEMM_FLAG_STAGE_K1) && !mn_a && !mn_b && d.K > atom_k &&
+               3 * (2 * atom_bytes + 16) + fixed_bytes <= props.smem_optin_bytes) {
+        atoms = 2;
+    }
+    const int tile_k = (int)(atoms * atom_k);
+    const int64_t stage_a = atoms * 128 * 128;      // 128 rows x 128 B per atom
+    const int64_t stage_b = atoms * (tile_n / cg) * 128;
     const int64_t stage_bytes = stage_a + stage_b;
     // Epilogue: TMA stores through a 32 KB staging area (default), or direct
     // row stores with no staging (on request).  On GB300 the staging area's
@@ -376,14 +393,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // waves of clusters, the last wave plus one full wave (sk_tiles >= clusters)
 // are split evenly along K over all clusters; the rest stays data-parallel.
 // Worth it only for long K (the fixup moves one fp32 tile per split).
-constexpr int kStreamKMinKBlocks = 16;
+constexpr int kStreamKMinKBlocks = 16;   // 128-byte K atoms
 
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
     info->stream_k_tiles = 0;
     info->workspace_bytes = 0;
     if (info->kernel != GEMM_KERNEL_PERSISTENT || (d.flags & GEMM_FLAG_NO_STREAM_K)) return;
     const int64_t clusters = info->grid / info->cta_group;
-    const int64_t nk = ceil_div(d.K, info->tile_k);
+    // the threshold counts 128-byte K atoms, whatever the stage depth
+    const int64_t atoms = std::max<int64_t>(info->tile_k * elem_bytes(d.dtype_a) / 128, 1);
+    const int64_t nk = ceil_div(d.K, info->tile_k) * atoms;
     if (clusters < 2 || nk < kStreamKMinKBlocks || info->num_tiles < clusters) return;
     const int64_t rem = info->num_tiles % clusters;
     if (rem == 0) return;
@@ -588,15 +607,17 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     if (!plan->maps_valid || plan->map_ptrs[0] != A || plan->map_ptrs[1] != B || plan->map_ptrs[2] != D) {
         plan->maps_valid = false;
         const bool mn_a = d.major_a == GEMM_MN_MAJOR, mn_b = d.major_b == GEMM_MN_MAJOR;
-        // K-major: (K, rows) boxes of tile_k x rows.  MN-major: (rows, K) boxes of 64 x tile_k.
+        // K-major: (K, rows) boxes of one 128-byte atom x rows (k_atoms per
+        // stage).  MN-major: (rows, K) boxes of 64 x tile_k.
+        const int atom_k = (int)(128 / eb_a);
         const bool ok_a = mn_a ? encode_map(&plan->maps[0], d.dtype_a, A, d.M, d.K, d.lda, batch_maps, d.stride_a,
                                             64, info.tile_k)
                                : encode_map(&plan->maps[0], d.dtype_a, A, d.K, d.M, d.lda, batch_maps, d.stride_a,
-                                            info.tile_k, 128);
+                                            atom_k, 128);
         const bool ok_b = mn_b ? encode_map(&plan->maps[1], d.dtype_b, B, d.N, d.K, d.ldb, batch_maps, d.stride_b,
                                             64, info.tile_k)
                                : encode_map(&plan->maps[1], d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b,
-                                            info.tile_k, info.tile_n / cg);
+                                            atom_k, info.tile_n / cg);
         if (!ok_a || !ok_b ||
             !encode_map(&plan->maps[2], d.dtype_d, D, d.N, d.M, d.ldd, batch_maps, d.stride_d, 128 / eb_d, 32)) {
             g_last_cuda_error = (int)cudaErrorInvalidValue;
@@ -624,6 +645,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.group_m = d.raster_group > 0 ? d.raster_group : kDefaultRasterGroup;
     p.batched = d.batch > 1 ? 1 : 0;
     p.tile_k = info.tile_k;
+    p.k_atoms = (int32_t)(info.tile_k * eb_a / 128);   // 128-byte K atoms per stage
     p.mma_kind = d.dtype_a == GEMM_TF32 ? dgb::kMmaKindTF32 : dgb::kMmaKindF16;
     // A/B formats: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = tf32
     p.mn_major_a = d.major_a == GEMM_MN_MAJOR;

@@ -49,6 +49,87 @@ constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 row
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = 192;
 
+// MMA issuer (one thread of the pair leader).  Per ring stage: wait for the
+// stage's data, issue four MMAs per 128-byte K atom (K16 of 16-bit elements
+// or K8 of tf32; ATOMS atoms per stage, rows x 128 B apart), commit the
+// stage back to the producer.  Per tile: wait for an empty accumulator
+// buffer first, commit it to the epilogue after the tile's last stage.
+// Issuing costs the thread about 45 cycles per MMA and 230 per barrier wait
+// (measured on GB300): at one atom per stage that is ~450 of the 512 cycles
+// the four MMAs of a 256 x 256 pair tile take, so the loop is kept lean.
+template <int CG, int ATOMS>
+__device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes,
+                                           uint32_t tmem_base, uint32_t full0, uint32_t empty0, uint32_t tfull0,
+                                           uint32_t tempty0, uint32_t drain_bar, volatile uint32_t* abort_flag,
+                                           int cluster_id, int num_clusters) {
+    const int S = p.stages;
+    const int TS = p.tmem_stages;
+    const uint64_t tmo = p.timeout_ns;
+    auto full = [&](int s) { return full0 + 8u * s; };
+    auto empty = [&](int s) { return empty0 + 8u * s; };
+    auto tfull = [&](int a) { return tfull0 + 8u * a; };
+    auto tempty = [&](int a) { return tempty0 + 8u * a; };
+    const uint64_t b_atom = (uint64_t)(p.tile_n / CG) * 8u;   // B atom stride in descriptor units
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool aborted = false;
+    bool issued_any = false;
+    WorkUnit u;
+    for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
+        const int t = u.tile;
+        if (!wait_phase<CG == 2>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
+            aborted = true;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+            if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+            const uint32_t sb = sa + p.stage_bytes_a;
+            // K-major: next MMA's K is 32 bytes along the row (+2 in the
+            // descriptor's address field); MN-major: 16 k-rows on (+128).
+            const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+            const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn(sb) : smem_desc_sw128(sb);
+            const uint64_t step_a = p.mn_major_a ? 128u : 2u;
+            const uint64_t step_b = p.mn_major_b ? 128u : 2u;
+#pragma unroll
+            for (int at = 0; at < ATOMS; ++at) {
+                // next atom: 128 rows (A) or tile_n / CG rows (B) x 128 B on
+                const uint64_t da_at = da + (uint64_t)at * (128u * 8u);
+                const uint64_t db_at = db + (uint64_t)at * b_atom;
+                const bool first = kb == u.kb0 && at == 0;
+                if (p.mma_kind == kMmaKindTF32) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32<CG>(d_tmem, da_at + 2u * kk, db_at + 2u * kk, p.idesc, !first || (kk != 0));
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16<CG>(d_tmem, da_at + step_a * kk, db_at + step_b * kk, p.idesc, !first || (kk != 0));
+                }
+            }
+            issued_any = true;
+            commit_to<CG>(empty(stage));
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (aborted) break;
+        commit_to<CG>(tfull(acc));
+        if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (aborted && issued_any) {
+        // Abort: make sure every MMA issued so far has finished before TMEM is freed.
+        commit_local<CG>(drain_bar);
+        wait_phase_drain(drain_bar, 0, tmo);
+    }
+}
+
 template <int CG, int OUT>
 __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_constant__ PersistentParams p) {
     constexpr int kOutBytes = (OUT == GEMM_F32) ? 4 : 2;
@@ -115,67 +196,26 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0)
-            producer_loop<CG>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
-                              num_clusters);
+        if (lane == 0) {
+            if (p.k_atoms == 2)
+                producer_loop<CG, 2>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
+                                     num_clusters);
+            else
+                producer_loop<CG, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
+                                     num_clusters);
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && leader) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            bool aborted = false;
-            bool issued_any = false;
-            WorkUnit u;
-            for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
-                const int t = u.tile;
-                if (!wait_phase<CG == 2>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma,
-                                         acc, t)) {
-                    aborted = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
-                    if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
-                        aborted = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                    const uint32_t sb = sa + p.stage_bytes_a;
-                    // K-major: next MMA's K is 32 bytes along the row (+2 in the
-                    // descriptor's address field); MN-major: 16 k-rows on (+128).
-                    const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
-                    const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn(sb) : smem_desc_sw128(sb);
-                    const uint64_t step_a = p.mn_major_a ? 128u : 2u;
-                    const uint64_t step_b = p.mn_major_b ? 128u : 2u;
-                    // four MMAs per stage: K16 of 16-bit elements or K8 of tf32
-                    if (p.mma_kind == kMmaKindTF32) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_tf32<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, (kb != u.kb0) || (kk != 0));
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f16<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc,
-                                        (kb != u.kb0) || (kk != 0));
-                    }
-                    issued_any = true;
-                    commit_to<CG>(empty(stage));
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
-                if (aborted) break;
-                commit_to<CG>(tfull(acc));
-                if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
-            }
-            if (aborted && issued_any) {
-                // Abort: make sure every MMA issued so far has finished before TMEM is freed.
-                commit_local<CG>(drain_bar);
-                wait_phase_drain(drain_bar, 0, tmo);
-            }
+            // the stage depth is a template argument: this thread is the
+            // kernel's tightest loop, so no per-stage branching on it
+            if (p.k_atoms == 2)
+                mma_issuer<CG, 2>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
+                                  abort_flag, cluster_id, num_clusters);
+            else
+                mma_issuer<CG, 1>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
+                                  abort_flag, cluster_id, num_clusters);
         }
         __syncwarp();
     } else {

@@ -124,17 +124,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Copy one operand's slice for one ring stage: `rows` rows (M or N) of
-// `tile_k` K elements.  K-major: one box of tile_k x rows.  MN-major: boxes of
-// 64 contiguous M/N elements x tile_k k-rows, one per 64 rows, 8 KB apart.
-template <int CG>
+// `tile_k` K elements.  K-major: `atoms` boxes of (tile_k / atoms) x rows, one
+// 128-byte swizzle atom column each, stored rows x 128 B apart.  MN-major
+// (atoms == 1): boxes of 64 contiguous M/N elements x tile_k k-rows, one per
+// 64 rows, 8 KB apart.
+template <int CG, int ATOMS = 1>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn_major,
                                              int rows, int row0, int kx, int b, bool batched, bool hint,
-                                             uint64_t policy) {
-    const int boxes = mn_major ? rows / 64 : 1;
+                                             uint64_t policy, int atom_k = 0) {
+    const int boxes = mn_major ? rows / 64 : ATOMS;
     for (int j = 0; j < boxes; ++j) {
-        const int x = mn_major ? row0 + 64 * j : kx;
+        const int x = mn_major ? row0 + 64 * j : (ATOMS == 1 ? kx : kx + j * atom_k);
         const int y = mn_major ? kx : row0;
-        const uint32_t d = dst + (uint32_t)j * kMNMajorBoxBytes;
+        const uint32_t d = dst + (uint32_t)j * (mn_major ? kMNMajorBoxBytes : (uint32_t)rows * 128u);
         if constexpr (CG == 1) {
             if (batched) {
                 if (hint) tma_load_3d_hint(d, map, bar, x, y, b, policy);
@@ -156,8 +158,10 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
 }
 
 // TMA producer (one thread).  `tile_k` is the ring stage depth in elements of
-// A/B (one 128-byte swizzle row: 64 for 16-bit, 128 for 8-bit types).
-template <int CG>
+// A/B: ATOMS 128-byte swizzle rows (one row: 64 for 16-bit, 128 for 8-bit
+// types).  Like the MMA issuer, this thread's loop is near its per-stage
+// budget at one atom per stage, so the atom count is a template argument.
+template <int CG, int ATOMS = 1>
 __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes, int tile_k,
                               uint32_t full0, uint32_t empty0, volatile uint32_t* abort_flag, uint32_t rank,
                               int cluster_id, int num_clusters) {
@@ -170,6 +174,7 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
     bool aborted = false;
     const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
     const int b_rows = p.tile_n / CG;
+    const int atom_k = tile_k / ATOMS;
     // Consecutive waves of a raster group reuse its A panels: keep them in L2.
     const bool keep_a = (p.l2_hints & kHintKeepA) != 0;
     const uint64_t pol_a = l2_policy_evict_last();
@@ -194,10 +199,10 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                 const uint32_t sb = sa + p.stage_bytes_a;
                 const int kx = kb * tile_k;
-                load_operand<CG>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0, keep_a,
-                                 pol_a);
-                load_operand<CG>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b, p.batched != 0, false,
-                                 pol_a);
+                load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
+                                        keep_a, pol_a, atom_k);
+                load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b, p.batched != 0,
+                                        false, pol_a, atom_k);
             }
             ++issued;
             if (++stage == S) { stage = 0; phase ^= 1u; }

@@ -83,6 +83,8 @@ typedef enum {
 #define GEMM_FLAG_NO_STREAM_K     (1u << 5)  /* data-parallel tiles only (no stream-K workspace) */
 #define GEMM_FLAG_EPILOGUE_DIRECT (1u << 6)  /* force direct row stores of D (no staging area) */
 #define GEMM_FLAG_EPILOGUE_TMA    (1u << 7)  /* force TMA stores of D through shared-memory staging */
+#define GEMM_FLAG_STAGE_K1        (1u << 8)  /* 16-bit/tf32 persistent kernel: one 128-byte K atom per ring stage */
+#define GEMM_FLAG_STAGE_K2        (1u << 9)  /* ... two 128-byte K atoms per ring stage (K-major operands only) */
 #define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
                                                 the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
 

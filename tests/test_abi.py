@@ -81,11 +81,32 @@ def test_headline_plan_is_pair_tiles():
     s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
     assert s == dg.GEMM_OK
     assert info.kernel == dg.GEMM_KERNEL_PERSISTENT
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 64)
+    # ring stages two 128-byte K atoms deep (128 bf16), three of them
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 128)
+    assert info.stages == 3 and info.stage_bytes == 2 * (128 * 128 + 128 * 128)
     assert info.num_tiles == 32 * 32
     assert info.grid == 152 and info.grid % 2 == 0
     assert info.tmem_cols <= 512 and info.tmem_stages * info.tile_n <= 512
     assert info.smem_bytes <= GB300.smem_optin_bytes
+
+
+def test_stage_depth_flags():
+    base = dict(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    s, info = query(flags=dg.GEMM_FLAG_STAGE_K1, **base)
+    assert s == dg.GEMM_OK and info.tile_k == 64 and info.stages == 6
+    s, info = query(flags=dg.GEMM_FLAG_STAGE_K1 | dg.GEMM_FLAG_STAGE_K2, **base)
+    assert s == dg.GEMM_ERR_INVALID_ARG
+    # MN-major operands keep one atom per stage; asking for two is refused
+    s, info = query(major_a=dg.GEMM_MN_MAJOR, **base)
+    assert s == dg.GEMM_OK and info.tile_k == 64
+    s, info = query(major_a=dg.GEMM_MN_MAJOR, flags=dg.GEMM_FLAG_STAGE_K2, **base)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
+    # K within one atom: one atom per stage
+    s, info = query(M=1024, N=1024, K=64, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, flags=dg.GEMM_FLAG_NO_SINGLE_CTA)
+    assert s == dg.GEMM_OK and info.tile_k == 64
+    # tf32: 32 elements per atom
+    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
+    assert s == dg.GEMM_OK and info.tile_k == 64
 
 
 def test_batched_plan():
@@ -192,7 +213,7 @@ def test_stream_k_plan():
 
 def test_variant_dtype_plans():
     s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
-    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and info.tile_k == 32
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and info.tile_k == 64   # two 32-element atoms
     s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, dtype_b=dg.GEMM_E5M2, dtype_d=dg.GEMM_BF16,
                     scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
     assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_FP8_BLOCK

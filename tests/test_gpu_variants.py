@@ -56,7 +56,7 @@ def run(prob, out, **kw):
 def test_tf32_integers_bit_exact(cg_flag, out):
     prob = inputs.make("square8192_bf16", M=600, N=712, K=1060, dist="ints", seed=71, dtype_in="tf32")
     got, dref, s, info = run(prob, out, flags=cg_flag)
-    assert info["tile_k"] == 32
+    assert info["tile_k"] in (32, 64)   # one or two 128-byte atoms of 32 tf32 (two if three stages fit)
     r = compare(got, dref, s, out, TOL_TF32, exact=True)
     if not r["ok"]:
         dump_on_failure("tf32_%s_%d" % (out, cg_flag), got=got, dref=dref, sabs=s)
@@ -85,3 +85,40 @@ def test_e5m2_quantised_normal():
     got, dref, s, info = run(prob, "bf16")
     r = compare(got, dref, s, "bf16", TOL_FP8)
     assert r["ok"], r
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("dtype_in,K", [("bf16", 1000), ("bf16", 64), ("f16", 200), ("tf32", 1060), ("tf32", 32)])
+def test_two_atom_stages_bit_exact(cg_flag, dtype_in, K):
+    """Ring stages two 128-byte K atoms deep: the second atom of the last
+    stage is partly (K = 1000, 200, 1060) or wholly (K = 64, 32) past K and
+    reads TMA's zero fill."""
+    prob = inputs.make("square8192_bf16", M=520, N=600, K=K, dist="ints", seed=73, dtype_in=dtype_in)
+    got, dref, s, info = run(prob, "f32", flags=cg_flag | dg.GEMM_FLAG_STAGE_K2 | dg.GEMM_FLAG_NO_SINGLE_CTA)
+    assert info["tile_k"] == (128 if dtype_in != "tf32" else 64)
+    assert info["kernel"] == dg.GEMM_KERNEL_PERSISTENT
+    r = compare(got, dref, s, "f32", TOL_TF32, exact=True)
+    if not r["ok"]:
+        dump_on_failure("k2_%s_%d_cg%d" % (dtype_in, K, info["cta_group"]), got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+
+
+def test_two_atom_stages_stream_k_random():
+    """Stream-K splits count K blocks of the deeper stage (sampled rows of
+    every tile row band against the oracle)."""
+    prob = inputs.make("square8192_bf16", M=2048, N=2560, K=2048, seed=74)
+    wl = prob.wl
+    A, B = prob.A.cuda(), prob.B.cuda()
+    D = torch.full((wl.M, wl.N), float("nan"), device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32,
+                        flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_STAGE_K2)
+    with dg.Plan(desc) as plan:
+        plan.run(A, B, D)
+        assert plan.sync_status()[0] == dg.GEMM_OK
+        info = plan.info.as_dict()
+    assert info["stream_k_tiles"] > 0 and info["tile_k"] == 128
+    rows = inputs.sample_rows(wl.M, 1, n_random=48, seed=2, tile_m=info["tile_m"])
+    dref, s = oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="bf16", dtype_b="bf16", rows=rows)
+    got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref.reshape(got.shape), s.reshape(got.shape), "f32", 2e-3)
+    assert r["ok"], (r, info)
