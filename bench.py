@@ -36,6 +36,7 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 PROFILE = os.path.join(ROOT, "profiles", "persistent_pair_square8192_bf16_f32.md")
 KERNEL_SOURCES = ["dense_gemm_blackwell_gb300/csrc/kernels_persistent.cu",
+                  "dense_gemm_blackwell_gb300/csrc/pipeline.cuh",
                   "dense_gemm_blackwell_gb300/csrc/ptx.cuh",
                   "dense_gemm_blackwell_gb300/csrc/common.cuh"]
 
