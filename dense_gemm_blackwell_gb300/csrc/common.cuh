@@ -118,7 +118,7 @@ struct PersistentParams {
     void* d_ptr;
     int64_t ldd, stride_d;
     float* sk_partials;       // [slot][cta rank][128 rows x tile_n], layout of sk_partial_index
-    uint32_t* sk_flags;       // [slot][cta rank][4 epilogue warps]
+    uint32_t* sk_flags;       // [slot][cta rank][8 epilogue warps]
 };
 
 constexpr uint32_t kHintKeepA = 1u;

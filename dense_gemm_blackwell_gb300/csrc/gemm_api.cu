@@ -36,8 +36,9 @@ using dgb::SingleParams;
 
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-constexpr int kPersistentThreads = 192;
-constexpr int64_t kStagingBytes = 4 * 2 * 32 * 128;   // 4 epilogue warps x 2 buffers x 4 KB
+constexpr int kPersistentThreads = 320;   // producer, MMA and 8 epilogue warps
+constexpr int kSkFlagsPerCta = 8;         // stream-K: one published flag per epilogue warp
+constexpr int64_t kStagingBytes = 8 * 32 * 128;   // 8 epilogue warps x one 4 KB buffer
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
 constexpr int kDefaultRasterGroup = 8;                 // m blocks per raster group (least DRAM traffic on GB300)
 
@@ -260,12 +261,26 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     const int chunk_cols = 128 / out_bytes;
     const int cg = choose_cta_group(d, props, d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64));
     int64_t tile_n = d.tile_n;
-    if (tile_n == 0) tile_n = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
-    if (tile_n % 16 != 0 || tile_n < 16 || tile_n > 256) return GEMM_ERR_UNSUPPORTED;
+    if (tile_n == 0) {
+        tile_n = d.N >= 256 ? 256 : std::max<int64_t>(round_up(d.N, 64), 64);
+        // SM pairs on long K take 512-wide tiles: each SM then loads 48 instead of
+        // 64 bytes of operands per 1024 MMA cycles, which its TMA path sustains
+        // (8192^3 bf16 on GB300: 20 % fewer cycles), unless they pad N more
+        // than 256-wide tiles do or the operands are MN-major.
+        const int64_t pad256 = round_up(d.N, 256) - d.N, pad512 = round_up(d.N, 512) - d.N;
+        if (cg == 2 && !mn_a && !mn_b && !(d.flags & GEMM_FLAG_STAGE_K2) && d.N >= 1024 &&
+            (pad512 - pad256) * 20 <= d.N)
+            tile_n = 512;
+    }
+    // 512-wide tiles: two N = 256 MMAs per K step into one 512-column
+    // accumulator (K-major operands, one K atom per stage)
+    const bool wide = tile_n == 512;
+    if (wide && (mn_a || mn_b || (d.flags & GEMM_FLAG_STAGE_K2))) return GEMM_ERR_UNSUPPORTED;
+    if (!wide && (tile_n % 16 != 0 || tile_n < 16 || tile_n > 256)) return GEMM_ERR_UNSUPPORTED;
     if (tile_n % chunk_cols != 0) return GEMM_ERR_UNSUPPORTED;     // epilogue writes 128-byte column chunks
     if ((tile_n / cg) % 8 != 0) return GEMM_ERR_UNSUPPORTED;      // B half-tile rows form 8-row swizzle atoms
     if (mn_b && (tile_n / cg) % 64 != 0) return GEMM_ERR_UNSUPPORTED;  // MN-major B: 64-column boxes
-    const int tmem_stages = 2;
+    const int tmem_stages = wide ? 1 : 2;
     const int64_t tmem_need = tmem_stages * tile_n;
     if (tmem_need > 512) return GEMM_ERR_RESOURCES;
     const int tmem_cols = pow2_at_least(tmem_need);
@@ -283,7 +298,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     int atoms = 1;
     if (d.flags & GEMM_FLAG_STAGE_K2) {
         atoms = 2;
-    } else if (!(d.flags & GEMM_FLAG_STAGE_K1) && !mn_a && !mn_b && d.K > atom_k &&
+    } else if (!(d.flags & GEMM_FLAG_STAGE_K1) && !wide && !mn_a && !mn_b && d.K > atom_k &&
                3 * (2 * atom_bytes + 16) + fixed_bytes <= props.smem_optin_bytes) {
         atoms = 2;
     }
@@ -406,10 +421,13 @@ void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
     if (clusters < 2 || nk < kStreamKMinKBlocks || info->num_tiles < clusters) return;
     const int64_t rem = info->num_tiles % clusters;
     if (rem == 0) return;
+    // 512-wide tiles: a partial is 256 KB per CTA to write and add back;
+    // worth it only when the last wave would leave most clusters idle
+    if (info->tile_n > 256 && 2 * rem >= clusters) return;
     info->stream_k_tiles = (int32_t)(clusters + rem);
-    // one partial slot per cluster: cta_group CTAs x 128 rows x tile_n fp32, plus 4 flags per CTA
+    // one partial slot per cluster: cta_group CTAs x 128 rows x tile_n fp32, plus a flag per epilogue warp
     const int64_t partial_bytes = clusters * info->cta_group * 128 * info->tile_n * 4;
-    const int64_t flag_bytes = round_up(clusters * info->cta_group * 4 * 4, 256);
+    const int64_t flag_bytes = round_up(clusters * info->cta_group * kSkFlagsPerCta * 4, 256);
     info->workspace_bytes = partial_bytes + flag_bytes;
 }
 
@@ -530,7 +548,8 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
     p->epoch = 0;
     // One allocation: status record (256 B), then stream-K flags, then partials.
     const int64_t flag_bytes = info.stream_k_tiles
-                                   ? round_up((int64_t)(info.grid / info.cta_group) * info.cta_group * 16, 256) : 0;
+                                   ? round_up((int64_t)(info.grid / info.cta_group) * info.cta_group *
+                                                  kSkFlagsPerCta * 4, 256) : 0;
     const size_t total = 256 + (size_t)info.workspace_bytes;
     void* mem = nullptr;
     if ((e = cudaMalloc(&mem, total)) != cudaSuccess) {
@@ -617,7 +636,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
         const bool ok_b = mn_b ? encode_map(&plan->maps[1], d.dtype_b, B, d.N, d.K, d.ldb, batch_maps, d.stride_b,
                                             64, info.tile_k)
                                : encode_map(&plan->maps[1], d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b,
-                                            atom_k, info.tile_n / cg);
+                                            atom_k, std::min(info.tile_n, 256) / cg);
         if (!ok_a || !ok_b ||
             !encode_map(&plan->maps[2], d.dtype_d, D, d.N, d.M, d.ldd, batch_maps, d.stride_d, 128 / eb_d, 32)) {
             g_last_cuda_error = (int)cudaErrorInvalidValue;
@@ -650,8 +669,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     // A/B formats: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = tf32
     p.mn_major_a = d.major_a == GEMM_MN_MAJOR;
     p.mn_major_b = d.major_b == GEMM_MN_MAJOR;
+    // one MMA covers at most 256 columns (512-wide tiles issue two)
     p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u),
-                              (uint32_t)info.tile_m, (uint32_t)info.tile_n, (uint32_t)p.mn_major_a,
+                              (uint32_t)info.tile_m, (uint32_t)std::min(info.tile_n, 256), (uint32_t)p.mn_major_a,
                               (uint32_t)p.mn_major_b);
     p.stage_bytes_a = (uint32_t)(128 * info.tile_k * eb_a);
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);

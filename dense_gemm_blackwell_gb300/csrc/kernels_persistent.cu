@@ -14,13 +14,17 @@
 //                       fresh accumulator), commits to the slot's empty barrier;
 //                       after the tile's last slice commits to the
 //                       accumulator's full barrier.
-//   warps 2..5        : epilogue.  Wait for a full accumulator, read it with
-//                       tcgen05.ld (one row per thread), hand the buffer back,
-//                       convert, stage 32x128 B chunks in swizzled shared
-//                       memory and write D with TMA stores (coalesced lines).
+//   warps 2..9        : epilogue.  Wait for a full accumulator, read it with
+//                       tcgen05.ld (one row per thread; two warps per 32-lane
+//                       quarter, each half of the columns), hand the buffer
+//                       back, convert, stage 32x128 B chunks in swizzled
+//                       shared memory and write D with TMA stores (coalesced
+//                       lines).
 //
 // Two accumulator buffers live in tensor memory, so the epilogue of tile t
-// overlaps the MMAs of tile t+1.  The grid is persistent: CTA (pair) c takes
+// overlaps the MMAs of tile t+1.  512-wide tiles (two N = 256 MMAs per K step)
+// fill all 512 columns with one accumulator: the MMAs of tile t+1 then wait
+// until every epilogue warp has loaded its last columns of tile t.  The grid is persistent: CTA (pair) c takes
 // tiles c, c+G, ... in a grouped raster that keeps a wave's A and B panels in L2.
 // Every thread follows the same tile sequence and leaves the loop together.
 //
@@ -46,8 +50,12 @@
 namespace dgb {
 
 constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
-constexpr int kEpilogueWarps = 4;
-constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 8;             // two per TMEM lane quarter, one half of the chunks each
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+// 32-column TMEM loads an epilogue warp holds in registers at once: as many as
+// fit the 168 registers a thread of a 10-warp CTA can have without spilling
+template <int OUT>
+__host__ __device__ constexpr int batch_loads() { return OUT == GEMM_F32 ? 3 : 2; }
 
 // MMA issuer (one thread of the pair leader).  Per ring stage: wait for the
 // stage's data, issue four MMAs per 128-byte K atom (K16 of 16-bit elements
@@ -57,7 +65,10 @@ constexpr int kThreads = 192;
 // Issuing costs the thread about 45 cycles per MMA and 230 per barrier wait
 // (measured on GB300): at one atom per stage that is ~450 of the 512 cycles
 // the four MMAs of a 256 x 256 pair tile take, so the loop is kept lean.
-template <int CG, int ATOMS>
+// HALVES = 2 (512-wide tiles): each K step is two N = 256 MMAs, into
+// accumulator columns [0, 256) and [256, 512), B rows of the second half
+// 256 / CG rows further on in the stage.
+template <int CG, int ATOMS, int HALVES>
 __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes,
                                            uint32_t tmem_base, uint32_t full0, uint32_t empty0, uint32_t tfull0,
                                            uint32_t tempty0, uint32_t drain_bar, volatile uint32_t* abort_flag,
@@ -105,14 +116,19 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                 const uint64_t da_at = da + (uint64_t)at * (128u * 8u);
                 const uint64_t db_at = db + (uint64_t)at * b_atom;
                 const bool first = kb == u.kb0 && at == 0;
-                if (p.mma_kind == kMmaKindTF32) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_tf32<CG>(d_tmem, da_at + 2u * kk, db_at + 2u * kk, p.idesc, !first || (kk != 0));
-                } else {
+                for (int h = 0; h < HALVES; ++h) {
+                    const uint32_t d_h = d_tmem + (uint32_t)(h * 256);
+                    const uint64_t db_h = db_at + (uint64_t)(h * (256 / CG) * 8);
+                    if (p.mma_kind == kMmaKindTF32) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f16<CG>(d_tmem, da_at + step_a * kk, db_at + step_b * kk, p.idesc, !first || (kk != 0));
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_tf32<CG>(d_h, da_at + 2u * kk, db_h + 2u * kk, p.idesc, !first || (kk != 0));
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16<CG>(d_h, da_at + step_a * kk, db_h + step_b * kk, p.idesc, !first || (kk != 0));
+                    }
                 }
             }
             issued_any = true;
@@ -143,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     const uint32_t stage_bytes = p.stage_bytes_a + p.stage_bytes_b;
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + (p.direct_store ? 0 : kEpilogueWarps * 2 * kStagingBytes));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + (p.direct_store ? 0 : kEpilogueWarps * kStagingBytes));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * TS + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -197,12 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            if (p.k_atoms == 2)
-                producer_loop<CG, 2>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
-                                     num_clusters);
+            if (p.tile_n > 256)
+                producer_loop<CG, 1, 2>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                        cluster_id, num_clusters);
+            else if (p.k_atoms == 2)
+                producer_loop<CG, 2, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                        cluster_id, num_clusters);
             else
-                producer_loop<CG, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
-                                     num_clusters);
+                producer_loop<CG, 1, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                        cluster_id, num_clusters);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -210,26 +229,40 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         if (lane == 0 && leader) {
             // the stage depth is a template argument: this thread is the
             // kernel's tightest loop, so no per-stage branching on it
-            if (p.k_atoms == 2)
-                mma_issuer<CG, 2>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
-                                  abort_flag, cluster_id, num_clusters);
+            if (p.tile_n > 256)
+                mma_issuer<CG, 1, 2>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
+                                     abort_flag, cluster_id, num_clusters);
+            else if (p.k_atoms == 2)
+                mma_issuer<CG, 2, 1>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
+                                     abort_flag, cluster_id, num_clusters);
             else
-                mma_issuer<CG, 1>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
-                                  abort_flag, cluster_id, num_clusters);
+                mma_issuer<CG, 1, 1>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,
+                                     abort_flag, cluster_id, num_clusters);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // Eight warps: warp w reads TMEM lanes [32 (w mod 4), +32) (its 32 rows)
+        // and owns half of the tile's output chunks, the lower half for warps
+        // 2..5.  It loads its chunks in batches of up to 128 columns into
+        // registers and hands the accumulator back right after its last
+        // tcgen05.ld of the tile, before staging and storing that batch, so
+        // tensor memory is held for one batch's stores at most (with a single
+        // 512-column accumulator that hold is what the MMA waits for).
         // D is written once and never read back here: let it leave L2 first.
         const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
         const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                 // TMEM lanes [32*wq, 32*wq+32) are this warp's
-        uint8_t* my_staging = staging + (warp - 2) * 2 * kStagingBytes;
+        const int half = (warp - 2) >> 2;
+        uint8_t* buf = staging + (warp - 2) * kStagingBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int stores = 0;                          // TMA stores issued; selects the staging buffer
         const int nchunks = p.tile_n / kChunkCols;
+        const int c_lo = half == 0 ? 0 : (nchunks + 1) / 2;      // this warp's chunks [c_lo, c_hi)
+        const int c_hi = half == 0 ? (nchunks + 1) / 2 : nchunks;
         constexpr int kSub = kChunkCols / 32;    // 32-column TMEM loads per output chunk
+        constexpr int kBatchLoads = batch_loads<OUT>();
+        constexpr int kBatchChunks = kBatchLoads / kSub;
         WorkUnit u;
         for (int idx = 0; next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
             const int t = u.tile;
@@ -251,12 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 if (lane == 0) arrive_leader<CG>(tempty(acc));
             };
             const size_t part_base = (size_t)(u.slot * CG + (int)rank) * 128 * p.tile_n / 4;   // in float4
-            uint32_t* flag = p.sk_flags + (u.slot * CG + (int)rank) * 4 + wq;
+            uint32_t* flag = p.sk_flags + (u.slot * CG + (int)rank) * kEpilogueWarps + half * 4 + wq;
 
             if (u.role == kUnitContributor) {
                 // Leave this K range's fp32 partial for the finisher, then publish it.
                 float4* part = reinterpret_cast<float4*>(p.sk_partials) + part_base;
-                for (int c32 = 0; c32 < p.tile_n / 32; ++c32) {
+                for (int c32 = c_lo * kSub; c32 < c_hi * kSub; ++c32) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_lane + c32 * 32, r);
                     tmem_wait_ld();
@@ -293,97 +326,107 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             // Chunks that hold at least one in-range column of an in-range row; the
             // rest of the tile (padding beyond M or N) is neither read nor stored.
             const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
-            if (n_valid == 0) release();
-            for (int c = 0; c < n_valid; ++c) {
-                uint32_t w[32];
-                float f[32 * kSub];
+            const int c_end = min(c_hi, n_valid);
+            if (c_lo >= c_end) release();
+            for (int c0 = c_lo; c0 < c_end; c0 += kBatchChunks) {
+                const int nc = min(kBatchChunks, c_end - c0);    // chunks in this batch
+                uint32_t r[kBatchLoads][32];
 #pragma unroll
-                for (int h = 0; h < kSub; ++h) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_lane + (c * kSub + h) * 32, r);
-                    tmem_wait_ld();
-                    tmem_reg_fence(r);
+                for (int q = 0; q < kBatchLoads; ++q)
+                    if (q < nc * kSub) tmem_ld_32x32b_x32(t_lane + (c0 * kSub + q) * 32, r[q]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) f[h * 32 + i] = __uint_as_float(r[i]);
-                }
-                if (c == n_valid - 1) release();
-                if (adds) {
+                for (int q = 0; q < kBatchLoads; ++q)
+                    if (q < nc * kSub) tmem_reg_fence(r[q]);
+                if (c0 + nc == c_end) release();
 #pragma unroll
-                    for (int h = 0; h < kSub; ++h) {
+                for (int cc = 0; cc < kBatchChunks; ++cc) {
+                    if (cc >= nc) break;
+                    const int c = c0 + cc;
+                    if (adds) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 q = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
-                            // own part (later K) + partial (earlier K): one fixed order
-                            f[h * 32 + 4 * j] += q.x;
-                            f[h * 32 + 4 * j + 1] += q.y;
-                            f[h * 32 + 4 * j + 2] += q.z;
-                            f[h * 32 + 4 * j + 3] += q.w;
-                        }
-                    }
-                }
-                if constexpr (OUT == GEMM_F32) {
+                        for (int h = 0; h < kSub; ++h) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(f[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = pack2<OUT>(f[2 * i], f[2 * i + 1]);
-                }
-                if (p.direct_store) {
-                    // This thread's row: 128 contiguous bytes, streaming stores.
-                    const int row = m0 + lane;
-                    const int x = n0 + c * kChunkCols;
-                    if (row < p.M) {
-                        uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
-                                       ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) * kOutBytes;
-                        if (x + kChunkCols <= p.N) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                __stcs(reinterpret_cast<int4*>(dst) + j,
-                                       make_int4((int)w[4 * j], (int)w[4 * j + 1], (int)w[4 * j + 2], (int)w[4 * j + 3]));
-                        } else {
-                            const int valid = p.N - x;
-#pragma unroll
-                            for (int e = 0; e < kChunkCols; ++e) {
-                                if (e < valid) {
-                                    if constexpr (OUT == GEMM_F32)
-                                        reinterpret_cast<uint32_t*>(dst)[e] = w[e];
-                                    else
-                                        reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
-                                }
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 qv = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                                // own part (later K) + partial (earlier K): one fixed order
+                                const int q = cc * kSub + h;
+                                r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);
+                                r[q][4 * j + 1] = __float_as_uint(__uint_as_float(r[q][4 * j + 1]) + qv.y);
+                                r[q][4 * j + 2] = __float_as_uint(__uint_as_float(r[q][4 * j + 2]) + qv.z);
+                                r[q][4 * j + 3] = __float_as_uint(__uint_as_float(r[q][4 * j + 3]) + qv.w);
                             }
                         }
                     }
-                    continue;
-                }
-                // The staging buffer written two stores ago must have been read by that store.
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                uint8_t* buf = my_staging + (stores & 1) * kStagingBytes;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+                    // 16-byte piece j (0..7) of this thread's 128-byte row segment
+                    auto piece = [&](int j) -> uint4 {
+                        if constexpr (OUT == GEMM_F32) {
+                            return make_uint4(r[cc][4 * j], r[cc][4 * j + 1], r[cc][4 * j + 2], r[cc][4 * j + 3]);
+                        } else {
+                            const int q = cc * kSub + (j >> 2), o = 8 * (j & 3);
+                            return make_uint4(pack2<OUT>(__uint_as_float(r[q][o]), __uint_as_float(r[q][o + 1])),
+                                              pack2<OUT>(__uint_as_float(r[q][o + 2]), __uint_as_float(r[q][o + 3])),
+                                              pack2<OUT>(__uint_as_float(r[q][o + 4]), __uint_as_float(r[q][o + 5])),
+                                              pack2<OUT>(__uint_as_float(r[q][o + 6]), __uint_as_float(r[q][o + 7])));
+                        }
+                    };
                     const int x = n0 + c * kChunkCols;
-                    if (stream_d) {
-                        if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m0, b, pol_d);
-                        else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m0, pol_d);
-                    } else {
-                        if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
-                        else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                    if (p.direct_store) {
+                        // This thread's row: 128 contiguous bytes, streaming stores.
+                        const int row = m0 + lane;
+                        if (row < p.M) {
+                            uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
+                                           ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) * kOutBytes;
+                            if (x + kChunkCols <= p.N) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<uint4*>(dst) + j, piece(j));
+                            } else {
+                                // ragged right edge: element by element, up to N
+                                const int valid = p.N - x;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const uint4 q = piece(j);
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) {
+                                        const uint32_t wv_k = k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
+                                        if constexpr (OUT == GEMM_F32) {
+                                            if (4 * j + k < valid) reinterpret_cast<uint32_t*>(dst)[4 * j + k] = wv_k;
+                                        } else {
+                                            const int e0 = 8 * j + 2 * k;
+                                            if (e0 < valid) reinterpret_cast<uint16_t*>(dst)[e0] = (uint16_t)(wv_k & 0xFFFFu);
+                                            if (e0 + 1 < valid) reinterpret_cast<uint16_t*>(dst)[e0 + 1] = (uint16_t)(wv_k >> 16);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        continue;
                     }
-                    bulk_commit_group();
+                    // The staging buffer's previous store must have read it.
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = piece(j);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (stream_d) {
+                            if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m0, b, pol_d);
+                            else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m0, pol_d);
+                        } else {
+                            if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
+                            else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                        }
+                        bulk_commit_group();
+                    }
                 }
-                ++stores;
             }
             if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }
-
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();

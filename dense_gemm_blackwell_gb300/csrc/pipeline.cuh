@@ -124,19 +124,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Copy one operand's slice for one ring stage: `rows` rows (M or N) of
-// `tile_k` K elements.  K-major: `atoms` boxes of (tile_k / atoms) x rows, one
-// 128-byte swizzle atom column each, stored rows x 128 B apart.  MN-major
-// (atoms == 1): boxes of 64 contiguous M/N elements x tile_k k-rows, one per
-// 64 rows, 8 KB apart.
+// `tile_k` K elements.  K-major: ATOMS boxes of (tile_k / ATOMS) x rows, one
+// 128-byte swizzle atom column each, `atom_stride` bytes apart (default
+// rows x 128 B).  MN-major (ATOMS == 1): boxes of 64 contiguous M/N elements
+// x tile_k k-rows, one per 64 rows, 8 KB apart.
 template <int CG, int ATOMS = 1>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn_major,
                                              int rows, int row0, int kx, int b, bool batched, bool hint,
-                                             uint64_t policy, int atom_k = 0) {
+                                             uint64_t policy, int atom_k = 0, uint32_t atom_stride = 0) {
     const int boxes = mn_major ? rows / 64 : ATOMS;
+    const uint32_t a_stride = atom_stride ? atom_stride : (uint32_t)rows * 128u;
     for (int j = 0; j < boxes; ++j) {
         const int x = mn_major ? row0 + 64 * j : (ATOMS == 1 ? kx : kx + j * atom_k);
         const int y = mn_major ? kx : row0;
-        const uint32_t d = dst + (uint32_t)j * (mn_major ? kMNMajorBoxBytes : (uint32_t)rows * 128u);
+        const uint32_t d = dst + (uint32_t)j * (mn_major ? kMNMajorBoxBytes : a_stride);
         if constexpr (CG == 1) {
             if (batched) {
                 if (hint) tma_load_3d_hint(d, map, bar, x, y, b, policy);
@@ -159,9 +160,11 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
 
 // TMA producer (one thread).  `tile_k` is the ring stage depth in elements of
 // A/B: ATOMS 128-byte swizzle rows (one row: 64 for 16-bit, 128 for 8-bit
-// types).  Like the MMA issuer, this thread's loop is near its per-stage
-// budget at one atom per stage, so the atom count is a template argument.
-template <int CG, int ATOMS = 1>
+// types).  HALVES = 2 for 512-wide tiles: B's tile rows are two 256-row
+// halves (one MMA each), every CTA loads its 256 / CG rows of each half; the
+// stage holds B as [atom][half][rows of the half].  Like the MMA issuer, this
+// thread's loop is near its per-stage budget, so both are template arguments.
+template <int CG, int ATOMS = 1, int HALVES = 1>
 __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes, int tile_k,
                               uint32_t full0, uint32_t empty0, volatile uint32_t* abort_flag, uint32_t rank,
                               int cluster_id, int num_clusters) {
@@ -201,8 +204,17 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 const int kx = kb * tile_k;
                 load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
                                         keep_a, pol_a, atom_k);
-                load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b, p.batched != 0,
-                                        false, pol_a, atom_k);
+                if constexpr (HALVES == 1) {
+                    load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
+                                            p.batched != 0, false, pol_a, atom_k);
+                } else {
+                    constexpr int kHalfRows = 256 / CG;
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false, kHalfRows,
+                                                nb * p.tile_n + h * 256 + (int)rank * kHalfRows, kx, b,
+                                                p.batched != 0, false, pol_a, atom_k, (uint32_t)b_rows * 128u);
+                }
             }
             ++issued;
             if (++stage == S) { stage = 0; phase ^= 1u; }

@@ -81,17 +81,22 @@ def test_headline_plan_is_pair_tiles():
     s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
     assert s == dg.GEMM_OK
     assert info.kernel == dg.GEMM_KERNEL_PERSISTENT
-    # ring stages two 128-byte K atoms deep (128 bf16), three of them
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 128)
-    assert info.stages == 3 and info.stage_bytes == 2 * (128 * 128 + 128 * 128)
-    assert info.num_tiles == 32 * 32
+    # 512-wide pair tiles (two N = 256 MMAs per K step, one 512-column
+    # accumulator), four ring stages of one 128-byte K atom (64 bf16)
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 512, 64)
+    assert info.stages == 4 and info.stage_bytes == 128 * 128 + 256 * 128
+    assert info.tmem_stages == 1 and info.tmem_cols == 512
+    assert info.num_tiles == 32 * 16
+    assert info.stream_k_tiles == 0      # 512 tiles over 76 pairs: the last wave is 74 % full
     assert info.grid == 152 and info.grid % 2 == 0
     assert info.tmem_cols <= 512 and info.tmem_stages * info.tile_n <= 512
     assert info.smem_bytes <= GB300.smem_optin_bytes
 
 
 def test_stage_depth_flags():
-    base = dict(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    base = dict(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, tile_n=256)
+    s, info = query(**base)
+    assert s == dg.GEMM_OK and info.tile_k == 128 and info.stages == 3
     s, info = query(flags=dg.GEMM_FLAG_STAGE_K1, **base)
     assert s == dg.GEMM_OK and info.tile_k == 64 and info.stages == 6
     s, info = query(flags=dg.GEMM_FLAG_STAGE_K1 | dg.GEMM_FLAG_STAGE_K2, **base)
@@ -105,8 +110,12 @@ def test_stage_depth_flags():
     s, info = query(M=1024, N=1024, K=64, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, flags=dg.GEMM_FLAG_NO_SINGLE_CTA)
     assert s == dg.GEMM_OK and info.tile_k == 64
     # tf32: 32 elements per atom
-    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
+    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32, tile_n=256)
     assert s == dg.GEMM_OK and info.tile_k == 64
+    # 512-wide tiles keep one atom per stage; two are refused
+    s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, tile_n=512,
+                    flags=dg.GEMM_FLAG_STAGE_K2)
+    assert s == dg.GEMM_ERR_UNSUPPORTED
 
 
 def test_batched_plan():
@@ -198,12 +207,17 @@ def test_fp8_block_plan():
 def test_stream_k_plan():
     """Tiles that do not fill whole waves: the last wave plus one full wave are
     split along K (stream-K), one fp32 partial slot per cluster."""
+    for kw in (dict(M=8192, N=8192, K=8192, tile_n=256),      # 1024 tiles over 76 pairs
+               dict(M=2048, N=5120, K=2048)):                 # 80 512-wide tiles: the last wave holds 4
+        s, info = query(dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, **kw)
+        assert s == dg.GEMM_OK
+        clusters = info.grid // info.cta_group
+        assert info.num_tiles % clusters != 0
+        assert info.stream_k_tiles == clusters + info.num_tiles % clusters, kw
+        assert info.workspace_bytes >= clusters * info.cta_group * 128 * info.tile_n * 4
+    # 512-wide tiles with a last wave at least half full stay data-parallel
     s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
-    assert s == dg.GEMM_OK
-    clusters = info.grid // info.cta_group
-    assert info.num_tiles % clusters != 0
-    assert info.stream_k_tiles == clusters + info.num_tiles % clusters
-    assert info.workspace_bytes >= clusters * info.cta_group * 128 * info.tile_n * 4
+    assert s == dg.GEMM_OK and info.tile_n == 512 and info.stream_k_tiles == 0
     # whole waves, short K, or the flag: data-parallel only, no workspace
     for kw in (dict(M=256 * 76, N=256, K=8192), dict(M=256, N=256, K=256, batch=512),
                dict(M=8192, N=8192, K=8192, flags=dg.GEMM_FLAG_NO_STREAM_K)):
@@ -213,7 +227,8 @@ def test_stream_k_plan():
 
 def test_variant_dtype_plans():
     s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
-    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and info.tile_k == 64   # two 32-element atoms
+    # 512-wide pair tiles, one 32-element atom per stage
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and (info.tile_n, info.tile_k) == (512, 32)
     s, info = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, dtype_b=dg.GEMM_E5M2, dtype_d=dg.GEMM_BF16,
                     scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
     assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_FP8_BLOCK

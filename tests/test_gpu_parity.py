@@ -157,7 +157,7 @@ def test_stream_k_integers_bit_exact(cg_flag, M, N, K, ctas, out):
     """Capping the clusters forces a partial last wave: its tiles are split
     along K between two clusters (contributor partial + finisher)."""
     prob = inputs.make("square8192_bf16", M=M, N=N, K=K, dist="ints", seed=17)
-    r, info = check_full(prob, out, exact=True, flags=cg_flag, max_ctas=ctas)
+    r, info = check_full(prob, out, exact=True, flags=cg_flag, max_ctas=ctas, tile_n=256)
     assert info["stream_k_tiles"] > 0
 
 
@@ -230,7 +230,7 @@ def check_sampled(name, out_dtype, rows_per_tile=None, **desc_kw):
 @pytest.mark.slow
 def test_full_square8192_bf16_f32():
     r, info = check_sampled("square8192_bf16", "f32")
-    assert info["cta_group"] == 2 and info["tile_n"] == 256
+    assert info["cta_group"] == 2 and info["tile_n"] == 512 and info["tmem_stages"] == 1   # 512-wide pair tiles
 
 
 @pytest.mark.slow

@@ -65,7 +65,7 @@ def test_tf32_integers_bit_exact(cg_flag, out):
 
 def test_tf32_random_and_stream_k():
     prob = inputs.make("square4096_bf16", M=1024, N=1024, K=2048, seed=72, dtype_in="tf32")
-    got, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
+    got, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10, tile_n=256)
     assert info["stream_k_tiles"] > 0
     r = compare(got, dref, s, "f32", TOL_TF32)
     assert r["ok"], r
@@ -118,6 +118,44 @@ def test_two_atom_stages_stream_k_random():
         info = plan.info.as_dict()
     assert info["stream_k_tiles"] > 0 and info["tile_k"] == 128
     rows = inputs.sample_rows(wl.M, 1, n_random=48, seed=2, tile_m=info["tile_m"])
+    dref, s = oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="bf16", dtype_b="bf16", rows=rows)
+    got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref.reshape(got.shape), s.reshape(got.shape), "f32", 2e-3)
+    assert r["ok"], (r, info)
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("dtype_in,out,epi", [("bf16", "f32", dg.GEMM_FLAG_EPILOGUE_TMA),
+                                             ("bf16", "f32", dg.GEMM_FLAG_EPILOGUE_DIRECT),
+                                             ("f16", "bf16", dg.GEMM_FLAG_EPILOGUE_TMA),
+                                             ("tf32", "f32", dg.GEMM_FLAG_EPILOGUE_DIRECT)])
+def test_wide_tiles_bit_exact(cg_flag, dtype_in, out, epi):
+    """512-wide tiles: two N = 256 MMAs per K step into one 512-column
+    accumulator.  N = 1104 leaves the third tile column mostly past N."""
+    prob = inputs.make("square8192_bf16", M=520, N=1104, K=400, dist="ints", seed=75, dtype_in=dtype_in)
+    got, dref, s, info = run(prob, out, flags=cg_flag | epi, tile_n=512)
+    assert info["tile_n"] == 512 and info["tmem_stages"] == 1 and info["tmem_cols"] == 512
+    r = compare(got, dref, s, out, TOL_TF32, exact=True)
+    if not r["ok"]:
+        dump_on_failure("wide_%s_%s_cg%d" % (dtype_in, out, info["cta_group"]), got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+
+
+@pytest.mark.parametrize("epi", [dg.GEMM_FLAG_EPILOGUE_TMA, dg.GEMM_FLAG_EPILOGUE_DIRECT])
+def test_wide_tiles_stream_k_random(epi):
+    """512-wide pair tiles with stream-K (sampled rows of every tile row band)."""
+    prob = inputs.make("square8192_bf16", M=2048, N=5120, K=2048, seed=76)
+    wl = prob.wl
+    A, B = prob.A.cuda(), prob.B.cuda()
+    D = torch.full((wl.M, wl.N), float("nan"), device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32,
+                        flags=dg.GEMM_FLAG_CTA_GROUP_2 | epi, tile_n=512)
+    with dg.Plan(desc) as plan:
+        plan.run(A, B, D)
+        assert plan.sync_status()[0] == dg.GEMM_OK
+        info = plan.info.as_dict()
+    assert info["stream_k_tiles"] > 0 and info["tile_n"] == 512
+    rows = inputs.sample_rows(wl.M, 1, n_random=48, seed=3, tile_m=info["tile_m"])
     dref, s = oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="bf16", dtype_b="bf16", rows=rows)
     got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
     r = compare(got, dref.reshape(got.shape), s.reshape(got.shape), "f32", 2e-3)
