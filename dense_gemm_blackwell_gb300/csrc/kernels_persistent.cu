@@ -52,6 +52,7 @@ namespace dgb {
 constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
 constexpr int kEpilogueWarps = 8;             // two per TMEM lane quarter, one half of the chunks each
 constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+constexpr int kWideLeadStages = 2;            // 512-wide tiles: left-half stages issued before the right half is free
 // 32-column TMEM loads an epilogue warp holds in registers at once: as many as
 // fit the 168 registers a thread of a 10-warp CTA can have without spilling
 template <int OUT>
@@ -67,7 +68,9 @@ __host__ __device__ constexpr int batch_loads() { return OUT == GEMM_F32 ? 3 : 2
 // the four MMAs of a 256 x 256 pair tile take, so the loop is kept lean.
 // HALVES = 2 (512-wide tiles): each K step is two N = 256 MMAs, into
 // accumulator columns [0, 256) and [256, 512), B rows of the second half
-// 256 / CG rows further on in the stage.
+// 256 / CG rows further on in the stage.  The two column halves are handed
+// back separately, so a tile starts with the left halves of its first
+// kWideLeadStages stages before it waits for the right half.
 template <int CG, int ATOMS, int HALVES>
 __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes,
                                            uint32_t tmem_base, uint32_t full0, uint32_t empty0, uint32_t tfull0,
@@ -79,7 +82,7 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
     auto full = [&](int s) { return full0 + 8u * s; };
     auto empty = [&](int s) { return empty0 + 8u * s; };
     auto tfull = [&](int a) { return tfull0 + 8u * a; };
-    auto tempty = [&](int a) { return tempty0 + 8u * a; };
+    auto tempty = [&](int a, int part) { return tempty0 + 8u * (2 * a + part); };
     const uint64_t b_atom = (uint64_t)(p.tile_n / CG) * 8u;   // B atom stride in descriptor units
     int stage = 0;
     uint32_t phase = 0;
@@ -90,19 +93,15 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
     WorkUnit u;
     for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
         const int t = u.tile;
-        if (!wait_phase<CG == 2>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
+        if (!wait_phase<CG == 2>(tempty(acc, 0), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
             aborted = true;
             break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
-            if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
-                aborted = true;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+        // The MMAs of one ring stage for accumulator halves [h0, h1).
+        auto issue_stage = [&](int st, int kb, int h0, int h1) {
+            const uint32_t sa = smem_u32(ring + (size_t)st * stage_bytes);
             const uint32_t sb = sa + p.stage_bytes_a;
             // K-major: next MMA's K is 32 bytes along the row (+2 in the
             // descriptor's address field); MN-major: 16 k-rows on (+128).
@@ -118,6 +117,7 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                 const bool first = kb == u.kb0 && at == 0;
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
+                    if (h < h0 || h >= h1) continue;
                     const uint32_t d_h = d_tmem + (uint32_t)(h * 256);
                     const uint64_t db_h = db_at + (uint64_t)(h * (256 / CG) * 8);
                     if (p.mma_kind == kMmaKindTF32) {
@@ -132,6 +132,43 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                 }
             }
             issued_any = true;
+        };
+        int kb = u.kb0;
+        if constexpr (HALVES == 2) {
+            // The epilogue hands back columns [0, 256) first: run the first
+            // stages' left-half MMAs while it still reads [256, 512).
+            const int lead = min(kWideLeadStages, u.kb1 - u.kb0);
+            int st = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < lead; ++i) {
+                if (!wait_phase<false>(full(st), ph, abort_flag, tmo, p.status, kRoleMma, st, t)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                issue_stage(st, u.kb0 + i, 0, 1);
+                if (++st == S) { st = 0; ph ^= 1u; }
+            }
+            if (aborted) break;
+            if (!wait_phase<CG == 2>(tempty(acc, 1), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            for (int i = 0; i < lead; ++i) {
+                issue_stage(stage, u.kb0 + i, 1, 2);
+                commit_to<CG>(empty(stage));
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+            kb = u.kb0 + lead;
+        }
+        for (; kb < u.kb1; ++kb) {
+            if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            issue_stage(stage, kb, 0, HALVES);
             commit_to<CG>(empty(stage));
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -160,18 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + (p.direct_store ? 0 : kEpilogueWarps * kStagingBytes));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * TS + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3 * TS + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8u * S;
     const uint32_t tfull0 = empty0 + 8u * S;
-    const uint32_t tempty0 = tfull0 + 8u * TS;
-    const uint32_t drain_bar = tempty0 + 8u * TS;
+    const uint32_t tempty0 = tfull0 + 8u * TS;        // two per accumulator: columns [0, 256), [256, 512)
+    const uint32_t drain_bar = tempty0 + 16u * TS;
     auto full = [&](int s) { return full0 + 8u * s; };
     auto empty = [&](int s) { return empty0 + 8u * s; };
     auto tfull = [&](int a) { return tfull0 + 8u * a; };
-    auto tempty = [&](int a) { return tempty0 + 8u * a; };
+    auto tempty = [&](int a, int part) { return tempty0 + 8u * (2 * a + part); };
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
@@ -185,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         }
         for (int a = 0; a < TS; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), CG * kEpilogueWarps);
+            mbar_init(tempty(a, 0), CG * kEpilogueWarps);
+            mbar_init(tempty(a, 1), CG * kEpilogueWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -242,24 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Eight warps: warp w reads TMEM lanes [32 (w mod 4), +32) (its 32 rows)
-        // and owns half of the tile's output chunks, the lower half for warps
-        // 2..5.  It loads its chunks in batches of up to 128 columns into
-        // registers and hands the accumulator back right after its last
-        // tcgen05.ld of the tile, before staging and storing that batch, so
-        // tensor memory is held for one batch's stores at most (with a single
-        // 512-column accumulator that hold is what the MMA waits for).
+        // Eight warps: warp w reads TMEM lanes [32 (w mod 4), +32) (its 32 rows).
+        // A tile's columns form one part, or two 256-column parts for 512-wide
+        // tiles, each handed back on its own barrier; the two warps of a lane
+        // quarter split every part's output chunks.  A warp loads its chunks
+        // of a part in register batches (the first batch takes the remainder,
+        // so the last is full) and hands the part back right after its last
+        // tcgen05.ld of it, before staging and storing that batch: with a
+        // single 512-column accumulator the next tile's MMAs wait for these
+        // hand-backs, the left part's first.
         // D is written once and never read back here: let it leave L2 first.
         const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
         const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                 // TMEM lanes [32*wq, 32*wq+32) are this warp's
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - 2) >> 2;       // which of the lane quarter's two warps
         uint8_t* buf = staging + (warp - 2) * kStagingBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         const int nchunks = p.tile_n / kChunkCols;
-        const int c_lo = half == 0 ? 0 : (nchunks + 1) / 2;      // this warp's chunks [c_lo, c_hi)
-        const int c_hi = half == 0 ? (nchunks + 1) / 2 : nchunks;
+        const int parts = p.tile_n > 256 ? 2 : 1;
+        const int cpp = nchunks / parts;         // chunks per part
+        const int split = (cpp + 1) / 2;         // a part's chunks [0, split) for warp half 0
         constexpr int kSub = kChunkCols / 32;    // 32-column TMEM loads per output chunk
         constexpr int kBatchLoads = batch_loads<OUT>();
         constexpr int kBatchChunks = kBatchLoads / kSub;
@@ -277,11 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
             const int m0 = mb * (128 * CG) + (int)rank * 128 + wq * 32;
             const int n0 = nb * p.tile_n;
-            auto release = [&]() {
-                // Every TMEM read of this tile by this warp is complete: hand the buffer back.
+            auto release = [&](int part) {
+                // Every TMEM read of this part by this warp is complete: hand it back.
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_leader<CG>(tempty(acc));
+                if (lane == 0) arrive_leader<CG>(tempty(acc, part));
+            };
+            auto release_all = [&]() {
+                for (int q = 0; q < parts; ++q) release(q);
             };
             const size_t part_base = (size_t)(u.slot * CG + (int)rank) * 128 * p.tile_n / 4;   // in float4
             uint32_t* flag = p.sk_flags + (u.slot * CG + (int)rank) * kEpilogueWarps + half * 4 + wq;
@@ -289,7 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             if (u.role == kUnitContributor) {
                 // Leave this K range's fp32 partial for the finisher, then publish it.
                 float4* part = reinterpret_cast<float4*>(p.sk_partials) + part_base;
-                for (int c32 = c_lo * kSub; c32 < c_hi * kSub; ++c32) {
+                for (int c32 = 0; c32 < nchunks * kSub; ++c32) {
+                    const int c = c32 / kSub, cp = c % cpp;
+                    if ((cp < split) != (half == 0)) continue;     // the other warp's chunk
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(t_lane + c32 * 32, r);
                     tmem_wait_ld();
@@ -300,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                             make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                 }
-                release();
+                release_all();
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) store_release_gpu(flag, p.epoch);
@@ -315,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     got = wait_flag(flag, p.epoch, abort_flag, tmo, p.status, kRoleEpilogue, u.slot, t);
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
-                    release();
+                    release_all();
                     break;
                 }
                 uint32_t v;   // every lane acquires the flag before reading the partial
@@ -326,100 +372,105 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             // Chunks that hold at least one in-range column of an in-range row; the
             // rest of the tile (padding beyond M or N) is neither read nor stored.
             const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
-            const int c_end = min(c_hi, n_valid);
-            if (c_lo >= c_end) release();
-            for (int c0 = c_lo; c0 < c_end; c0 += kBatchChunks) {
-                const int nc = min(kBatchChunks, c_end - c0);    // chunks in this batch
-                uint32_t r[kBatchLoads][32];
+            for (int pt = 0; pt < parts; ++pt) {
+                const int c_lo = pt * cpp + (half == 0 ? 0 : split);          // this warp's chunks of the part
+                const int c_end = min(pt * cpp + (half == 0 ? split : cpp), n_valid);
+                if (c_lo >= c_end) release(pt);
+                const int first_nc = (c_end - c_lo) % kBatchChunks;
+                for (int c0 = c_lo; c0 < c_end;) {
+                    const int nc = (c0 == c_lo && first_nc) ? first_nc : kBatchChunks;   // chunks in this batch
+                    uint32_t r[kBatchLoads][32];
 #pragma unroll
-                for (int q = 0; q < kBatchLoads; ++q)
-                    if (q < nc * kSub) tmem_ld_32x32b_x32(t_lane + (c0 * kSub + q) * 32, r[q]);
-                tmem_wait_ld();
+                    for (int q = 0; q < kBatchLoads; ++q)
+                        if (q < nc * kSub) tmem_ld_32x32b_x32(t_lane + (c0 * kSub + q) * 32, r[q]);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < kBatchLoads; ++q)
-                    if (q < nc * kSub) tmem_reg_fence(r[q]);
-                if (c0 + nc == c_end) release();
+                    for (int q = 0; q < kBatchLoads; ++q)
+                        if (q < nc * kSub) tmem_reg_fence(r[q]);
+                    if (c0 + nc == c_end) release(pt);
 #pragma unroll
-                for (int cc = 0; cc < kBatchChunks; ++cc) {
-                    if (cc >= nc) break;
-                    const int c = c0 + cc;
-                    if (adds) {
+                    for (int cc = 0; cc < kBatchChunks; ++cc) {
+                        if (cc >= nc) break;
+                        const int c = c0 + cc;
+                        if (adds) {
 #pragma unroll
-                        for (int h = 0; h < kSub; ++h) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float4 qv = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
-                                // own part (later K) + partial (earlier K): one fixed order
-                                const int q = cc * kSub + h;
-                                r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);
-                                r[q][4 * j + 1] = __float_as_uint(__uint_as_float(r[q][4 * j + 1]) + qv.y);
-                                r[q][4 * j + 2] = __float_as_uint(__uint_as_float(r[q][4 * j + 2]) + qv.z);
-                                r[q][4 * j + 3] = __float_as_uint(__uint_as_float(r[q][4 * j + 3]) + qv.w);
-                            }
-                        }
-                    }
-                    // 16-byte piece j (0..7) of this thread's 128-byte row segment
-                    auto piece = [&](int j) -> uint4 {
-                        if constexpr (OUT == GEMM_F32) {
-                            return make_uint4(r[cc][4 * j], r[cc][4 * j + 1], r[cc][4 * j + 2], r[cc][4 * j + 3]);
-                        } else {
-                            const int q = cc * kSub + (j >> 2), o = 8 * (j & 3);
-                            return make_uint4(pack2<OUT>(__uint_as_float(r[q][o]), __uint_as_float(r[q][o + 1])),
-                                              pack2<OUT>(__uint_as_float(r[q][o + 2]), __uint_as_float(r[q][o + 3])),
-                                              pack2<OUT>(__uint_as_float(r[q][o + 4]), __uint_as_float(r[q][o + 5])),
-                                              pack2<OUT>(__uint_as_float(r[q][o + 6]), __uint_as_float(r[q][o + 7])));
-                        }
-                    };
-                    const int x = n0 + c * kChunkCols;
-                    if (p.direct_store) {
-                        // This thread's row: 128 contiguous bytes, streaming stores.
-                        const int row = m0 + lane;
-                        if (row < p.M) {
-                            uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
-                                           ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) * kOutBytes;
-                            if (x + kChunkCols <= p.N) {
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<uint4*>(dst) + j, piece(j));
-                            } else {
-                                // ragged right edge: element by element, up to N
-                                const int valid = p.N - x;
+                            for (int h = 0; h < kSub; ++h) {
 #pragma unroll
                                 for (int j = 0; j < 8; ++j) {
-                                    const uint4 q = piece(j);
+                                    const float4 qv = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                                    // own part (later K) + partial (earlier K): one fixed order
+                                    const int q = cc * kSub + h;
+                                    r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);
+                                    r[q][4 * j + 1] = __float_as_uint(__uint_as_float(r[q][4 * j + 1]) + qv.y);
+                                    r[q][4 * j + 2] = __float_as_uint(__uint_as_float(r[q][4 * j + 2]) + qv.z);
+                                    r[q][4 * j + 3] = __float_as_uint(__uint_as_float(r[q][4 * j + 3]) + qv.w);
+                                }
+                            }
+                        }
+                        // 16-byte piece j (0..7) of this thread's 128-byte row segment
+                        auto piece = [&](int j) -> uint4 {
+                            if constexpr (OUT == GEMM_F32) {
+                                return make_uint4(r[cc][4 * j], r[cc][4 * j + 1], r[cc][4 * j + 2], r[cc][4 * j + 3]);
+                            } else {
+                                const int q = cc * kSub + (j >> 2), o = 8 * (j & 3);
+                                return make_uint4(pack2<OUT>(__uint_as_float(r[q][o]), __uint_as_float(r[q][o + 1])),
+                                                  pack2<OUT>(__uint_as_float(r[q][o + 2]), __uint_as_float(r[q][o + 3])),
+                                                  pack2<OUT>(__uint_as_float(r[q][o + 4]), __uint_as_float(r[q][o + 5])),
+                                                  pack2<OUT>(__uint_as_float(r[q][o + 6]), __uint_as_float(r[q][o + 7])));
+                            }
+                        };
+                        const int x = n0 + c * kChunkCols;
+                        if (p.direct_store) {
+                            // This thread's row: 128 contiguous bytes, streaming stores.
+                            const int row = m0 + lane;
+                            if (row < p.M) {
+                                uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
+                                               ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) * kOutBytes;
+                                if (x + kChunkCols <= p.N) {
 #pragma unroll
-                                    for (int k = 0; k < 4; ++k) {
-                                        const uint32_t wv_k = k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
-                                        if constexpr (OUT == GEMM_F32) {
-                                            if (4 * j + k < valid) reinterpret_cast<uint32_t*>(dst)[4 * j + k] = wv_k;
-                                        } else {
-                                            const int e0 = 8 * j + 2 * k;
-                                            if (e0 < valid) reinterpret_cast<uint16_t*>(dst)[e0] = (uint16_t)(wv_k & 0xFFFFu);
-                                            if (e0 + 1 < valid) reinterpret_cast<uint16_t*>(dst)[e0 + 1] = (uint16_t)(wv_k >> 16);
+                                    for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<uint4*>(dst) + j, piece(j));
+                                } else {
+                                    // ragged right edge: element by element, up to N
+                                    const int valid = p.N - x;
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) {
+                                        const uint4 q = piece(j);
+#pragma unroll
+                                        for (int k = 0; k < 4; ++k) {
+                                            const uint32_t wv_k = k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
+                                            if constexpr (OUT == GEMM_F32) {
+                                                if (4 * j + k < valid) reinterpret_cast<uint32_t*>(dst)[4 * j + k] = wv_k;
+                                            } else {
+                                                const int e0 = 8 * j + 2 * k;
+                                                if (e0 < valid) reinterpret_cast<uint16_t*>(dst)[e0] = (uint16_t)(wv_k & 0xFFFFu);
+                                                if (e0 + 1 < valid) reinterpret_cast<uint16_t*>(dst)[e0 + 1] = (uint16_t)(wv_k >> 16);
+                                            }
                                         }
                                     }
                                 }
                             }
+                            continue;
                         }
-                        continue;
-                    }
-                    // The staging buffer's previous store must have read it.
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
+                        // The staging buffer's previous store must have read it.
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = piece(j);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (stream_d) {
-                            if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m0, b, pol_d);
-                            else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m0, pol_d);
-                        } else {
-                            if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
-                            else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = piece(j);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (stream_d) {
+                                if (p.batched) tma_store_3d_hint(&p.tmap_d, smem_u32(buf), x, m0, b, pol_d);
+                                else tma_store_2d_hint(&p.tmap_d, smem_u32(buf), x, m0, pol_d);
+                            } else {
+                                if (p.batched) tma_store_3d(&p.tmap_d, smem_u32(buf), x, m0, b);
+                                else tma_store_2d(&p.tmap_d, smem_u32(buf), x, m0);
+                            }
+                            bulk_commit_group();
                         }
-                        bulk_commit_group();
                     }
+                    c0 += nc;
                 }
             }
             if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
