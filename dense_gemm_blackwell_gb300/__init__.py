@@ -39,6 +39,7 @@ GEMM_FLAG_EPILOGUE_DIRECT = 1 << 6
 GEMM_FLAG_EPILOGUE_TMA = 1 << 7
 GEMM_FLAG_STAGE_K1 = 1 << 8
 GEMM_FLAG_STAGE_K2 = 1 << 9
+GEMM_FLAG_ACCUM_F16 = 1 << 10
 GEMM_FLAG_TEST_DROP_LOAD = 1 << 30
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")

@@ -57,13 +57,14 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128_mn(uint32_t smem_addr) {
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 / kind::f8f6f4 (public PTX ISA):
-//   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
+//   [4,6) D format (0 = f16, 1 = f32)   [7,10) A format   [10,13) B format
 //   [15] A major (0 = K)       [16] B major      [17,23) N >> 3   [24,29) M >> 4
 // A/B format for kind::f16: 0 = f16, 1 = bf16; for kind::f8f6f4: 0 = e4m3.
 // kind::tf32: 2 = tf32.  kind::f8f6f4: 0 = e4m3, 1 = e5m2 (A and B independently).
 __host__ __device__ constexpr uint32_t make_idesc2(uint32_t a_format, uint32_t b_format, uint32_t m, uint32_t n,
-                                                   uint32_t a_mn_major = 0, uint32_t b_mn_major = 0) {
-    return (1u << 4) | (a_format << 7) | (b_format << 10) | (a_mn_major << 15) |
+                                                   uint32_t a_mn_major = 0, uint32_t b_mn_major = 0,
+                                                   uint32_t d_format = 1) {
+    return (d_format << 4) | (a_format << 7) | (b_format << 10) | (a_mn_major << 15) |
            (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m, uint32_t n,
@@ -98,6 +99,7 @@ struct PersistentParams {
     uint32_t mma_kind;        // kMmaKindF16 or kMmaKindTF32 (16-bit kernel only)
     int32_t mn_major_a;       // 1: A is M-contiguous (loaded as 64x64 boxes, MN-major descriptor)
     int32_t mn_major_b;       // 1: B is N-contiguous
+    int32_t acc_f16;          // 1: the accumulator is fp16 (one per 32-bit TMEM column, low half)
     uint32_t idesc;
     uint32_t stage_bytes_a;   // per CTA
     uint32_t stage_bytes_b;   // per CTA

@@ -241,8 +241,12 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
         return GEMM_OK;
     }
 
+    // fp16 accumulation: f16 inputs, persistent kernel, data-parallel tiles
+    const bool acc16 = (d.flags & GEMM_FLAG_ACCUM_F16) != 0;
+    if (acc16 && (d.dtype_a != GEMM_F16 || d.dtype_b != GEMM_F16 || (d.flags & GEMM_FLAG_SINGLE_CTA)))
+        return GEMM_ERR_UNSUPPORTED;
     const bool want_single = (d.flags & GEMM_FLAG_SINGLE_CTA) != 0;
-    const bool allow_single = (d.flags & GEMM_FLAG_NO_SINGLE_CTA) == 0 &&
+    const bool allow_single = !acc16 && (d.flags & GEMM_FLAG_NO_SINGLE_CTA) == 0 &&
                               (d.flags & (GEMM_FLAG_CTA_GROUP_1 | GEMM_FLAG_CTA_GROUP_2)) == 0 &&
                               d.tile_n == 0 && d.stages == 0;
     if (want_single) {
@@ -415,7 +419,7 @@ constexpr int kStreamKMinKBlocks = 16;   // 128-byte K atoms
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
     info->stream_k_tiles = 0;
     info->workspace_bytes = 0;
-    if (info->kernel != GEMM_KERNEL_PERSISTENT || (d.flags & GEMM_FLAG_NO_STREAM_K)) return;
+    if (info->kernel != GEMM_KERNEL_PERSISTENT || (d.flags & (GEMM_FLAG_NO_STREAM_K | GEMM_FLAG_ACCUM_F16))) return;
     const int64_t clusters = info->grid / info->cta_group;
     // the threshold counts 128-byte K atoms, whatever the stage depth
     const int64_t atoms = std::max<int64_t>(info->tile_k * elem_bytes(d.dtype_a) / 128, 1);
@@ -672,9 +676,10 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.mn_major_a = d.major_a == GEMM_MN_MAJOR;
     p.mn_major_b = d.major_b == GEMM_MN_MAJOR;
     // one MMA covers at most 256 columns (512-wide tiles issue two)
-    p.idesc = dgb::make_idesc(d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u),
-                              (uint32_t)info.tile_m, (uint32_t)std::min(info.tile_n, 256), (uint32_t)p.mn_major_a,
-                              (uint32_t)p.mn_major_b);
+    const uint32_t fmt = d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u);
+    p.acc_f16 = (d.flags & GEMM_FLAG_ACCUM_F16) ? 1 : 0;
+    p.idesc = dgb::make_idesc2(fmt, fmt, (uint32_t)info.tile_m, (uint32_t)std::min(info.tile_n, 256),
+                               (uint32_t)p.mn_major_a, (uint32_t)p.mn_major_b, p.acc_f16 ? 0u : 1u);
     p.stage_bytes_a = (uint32_t)(128 * info.tile_k * eb_a);
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * info.tile_k * eb_b);
     p.flags = d.flags;

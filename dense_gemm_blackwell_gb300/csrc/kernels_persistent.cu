@@ -388,6 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     for (int q = 0; q < kBatchLoads; ++q)
                         if (q < nc * kSub) tmem_reg_fence(r[q]);
                     if (c0 + nc == c_end) release(pt);
+                    if (p.acc_f16) {
+                        // fp16 accumulator: the value is the low half of each 32-bit cell
+#pragma unroll
+                        for (int q = 0; q < kBatchLoads; ++q)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                r[q][i] = __float_as_uint(__half2float(__ushort_as_half((unsigned short)(r[q][i] & 0xFFFFu))));
+                    }
 #pragma unroll
                     for (int cc = 0; cc < kBatchChunks; ++cc) {
                         if (cc >= nc) break;

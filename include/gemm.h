@@ -85,6 +85,10 @@ typedef enum {
 #define GEMM_FLAG_EPILOGUE_TMA    (1u << 7)  /* force TMA stores of D through shared-memory staging */
 #define GEMM_FLAG_STAGE_K1        (1u << 8)  /* 16-bit/tf32 persistent kernel: one 128-byte K atom per ring stage */
 #define GEMM_FLAG_STAGE_K2        (1u << 9)  /* ... two 128-byte K atoms per ring stage (K-major operands only) */
+#define GEMM_FLAG_ACCUM_F16       (1u << 10) /* f16 A and B only: accumulate in fp16 in tensor memory ("half inputs
+                                                with a half or float accumulator", cuBLASDx "API Card: Blackwell
+                                                Pipeline (tcgen05)", precision list); persistent kernel, no
+                                                stream-K; partial sums must stay within fp16's range */
 #define GEMM_FLAG_TEST_DROP_LOAD  (1u << 30) /* test only: the producer skips one stage's load so
                                                 the consumer's bounded wait expires (GEMM_ERR_TIMEOUT) */
 

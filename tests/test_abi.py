@@ -237,3 +237,17 @@ def test_variant_dtype_plans():
     assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT
     s, _ = query(M=64, N=64, K=64, dtype_a=dg.GEMM_BF16, dtype_b=dg.GEMM_E4M3)
     assert s == dg.GEMM_ERR_UNSUPPORTED
+
+
+def test_fp16_accumulation_plans():
+    """fp16 accumulation: f16 inputs only, persistent kernel, data-parallel tiles."""
+    f = dg.GEMM_FLAG_ACCUM_F16
+    s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F16, flags=f)
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT and info.stream_k_tiles == 0
+    s, info = query(M=128, N=64, K=64, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F32, flags=f)   # single-CTA size
+    assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_PERSISTENT
+    for kw in (dict(dtype_a=dg.GEMM_BF16), dict(dtype_a=dg.GEMM_TF32),
+               dict(dtype_a=dg.GEMM_F16, flags=f | dg.GEMM_FLAG_SINGLE_CTA)):
+        kw.setdefault("flags", f)
+        s, _ = query(M=1024, N=1024, K=1024, dtype_d=dg.GEMM_F32, **kw)
+        assert s == dg.GEMM_ERR_UNSUPPORTED, kw

@@ -160,3 +160,37 @@ def test_wide_tiles_stream_k_random(epi):
     got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
     r = compare(got, dref.reshape(got.shape), s.reshape(got.shape), "f32", 2e-3)
     assert r["ok"], (r, info)
+
+
+@pytest.mark.parametrize("cg_flag,N", [(dg.GEMM_FLAG_CTA_GROUP_1, 600), (dg.GEMM_FLAG_CTA_GROUP_2, 600),
+                                       (dg.GEMM_FLAG_CTA_GROUP_2, 2048)])
+@pytest.mark.parametrize("out", ["f16", "f32"])
+def test_fp16_accumulation_integers_bit_exact(cg_flag, N, out):
+    """fp16 accumulator: integer inputs in [-3, 3] and K = 192 keep every
+    partial sum an integer of magnitude <= 1728, exact in fp16, so the result
+    is the exact product.  N = 2048 takes 512-wide pair tiles."""
+    prob = inputs.make("batched256_f16", M=520, N=N, K=192, batch=1, dist="ints", seed=77)
+    got, dref, s, info = run(prob, out, flags=cg_flag | dg.GEMM_FLAG_ACCUM_F16)
+    assert info["kernel"] == dg.GEMM_KERNEL_PERSISTENT and info["stream_k_tiles"] == 0
+    r = compare(got, dref, s, out, 0.0, exact=True)
+    if not r["ok"]:
+        dump_on_failure("acc16_%s_%d_cg%d" % (out, N, info["cta_group"]), got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+
+
+def test_fp16_accumulation_random_within_bound_and_differs_from_fp32():
+    """Random f16 inputs, K = 512: with the running sum rounded to fp16 at most
+    once per 8 products (the tensor core rounds once per K16 instruction or
+    less often), |D - exact| <= (K / 8) 2^-11 S.  The fp32-accumulated product
+    of the same inputs must differ somewhere, or the flag did not take effect."""
+    K = 512
+    prob = inputs.make("batched256_f16", M=512, N=1024, K=K, batch=1, seed=78)
+    got16, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_ACCUM_F16)
+    r = compare(got16, dref, s, "f32", (K / 8) * 2.0 ** -11)
+    assert r["ok"], (r, info)
+    got32, _, _, _ = run(prob, "f32")
+    assert compare(got32, dref, s, "f32", 2e-3)["ok"]
+    assert (got16 != got32).any()
+    # and fp32 accumulation is the closer of the two
+    import numpy as np
+    assert np.abs(got32 - dref).max() < np.abs(got16 - dref).max()
