@@ -40,11 +40,13 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t smem_addr) {
 }
 
 // MN-major operand (M or N contiguous in memory) with the 128-byte swizzle:
-// each 128-byte row holds 64 consecutive M (or N) elements of one k, eight
-// k-rows form a 1024-byte atom.  The tile is stored as TMA boxes of 64
-// elements x 64 k-rows (8 KB), side by side along M/N.  Leading-dim offset =
-// 8 KB between 64-element atoms along M/N; stride-dim offset = 1024 B between
-// groups of 8 k-rows.  One K16 MMA spans 16 k-rows: +2048 B per MMA.
+// each 128-byte row holds 128 bytes of consecutive M (or N) elements of one k
+// (64 16-bit or 128 8-bit elements), eight k-rows form a 1024-byte atom.  The
+// tile is stored as TMA boxes of one such row width x tile_k k-rows, side by
+// side along M/N.  Leading-dim offset = the box size (8 KB for 16-bit,
+// 64 k-rows; 16 KB for 8-bit, 128 k-rows) between atoms along M/N; stride-dim
+// offset = 1024 B between groups of 8 k-rows.  One MMA spans 16 (K16) or 32
+// (K32) k-rows: +2048 or +4096 B per MMA.
 constexpr uint32_t kMNMajorBoxBytes = 64 * 128;
 constexpr uint64_t kSmemDescSw128MNMajorBase =
     (uint64_t(kMNMajorBoxBytes >> 4) << 16) |   // LBO: next 64 elements of M/N
@@ -54,6 +56,12 @@ constexpr uint64_t kSmemDescSw128MNMajorBase =
 
 __host__ __device__ constexpr uint64_t smem_desc_sw128_mn(uint32_t smem_addr) {
     return kSmemDescSw128MNMajorBase | uint64_t((smem_addr >> 4) & 0x3FFFu);
+}
+
+// Same with a given leading-dim offset (the MN-major box size in bytes).
+__host__ __device__ constexpr uint64_t smem_desc_sw128_mn_lbo(uint32_t smem_addr, uint32_t lbo_bytes) {
+    return (uint64_t(lbo_bytes >> 4) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
+           (uint64_t(2) << 61) | uint64_t((smem_addr >> 4) & 0x3FFFu);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 / kind::f8f6f4 (public PTX ISA):
@@ -100,6 +108,7 @@ struct PersistentParams {
     int32_t mn_major_a;       // 1: A is M-contiguous (loaded as 64x64 boxes, MN-major descriptor)
     int32_t mn_major_b;       // 1: B is N-contiguous
     int32_t acc_f16;          // 1: the accumulator is fp16 (one per 32-bit TMEM column, low half)
+    int32_t mn_box_elems;     // MN-major boxes: elements along M/N per 128-byte row (64 or 128)
     uint32_t idesc;
     uint32_t stage_bytes_a;   // per CTA
     uint32_t stage_bytes_b;   // per CTA

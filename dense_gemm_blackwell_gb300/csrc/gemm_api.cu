@@ -178,6 +178,8 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
         if (cg == 2 && !(d.M > 128 && ceil_div(d.M, 256) * ceil_div(d.N, tile_n) * d.batch >= props.sm_count / 2))
             cg = 1;
     }
+    // MN-major B: boxes of 128 contiguous N elements, a whole number per CTA
+    if (d.major_b == GEMM_MN_MAJOR && (tile_n / cg) % 128 != 0) return GEMM_ERR_UNSUPPORTED;
     const int tile_k = 128;
     const int partials = (int)(512 / tile_n);
     const int64_t stage_bytes = 128 * tile_k + (tile_n / cg) * tile_k;
@@ -259,7 +261,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     // MN-major operands: 16-bit inputs only (tf32 needs K-major operands; the
     // block-scaled kernel is K-major).
     const bool mn_a = d.major_a == GEMM_MN_MAJOR, mn_b = d.major_b == GEMM_MN_MAJOR;
-    if ((mn_a || mn_b) && !is16(d.dtype_a)) return GEMM_ERR_UNSUPPORTED;
+    if ((mn_a || mn_b) && !is16(d.dtype_a) && !is8(d.dtype_a)) return GEMM_ERR_UNSUPPORTED;
     if (is8(d.dtype_a)) return plan_fp8(d, props, info);
     const int out_bytes = elem_bytes(d.dtype_d);
     const int chunk_cols = 128 / out_bytes;
@@ -636,11 +638,11 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
         // stage).  MN-major: (rows, K) boxes of 64 x tile_k.
         const int atom_k = (int)(128 / eb_a);
         const bool ok_a = mn_a ? encode_map(&plan->maps[0], d.dtype_a, A, d.M, d.K, d.lda, batch_maps, d.stride_a,
-                                            64, info.tile_k)
+                                            (int)(128 / eb_a), info.tile_k)
                                : encode_map(&plan->maps[0], d.dtype_a, A, d.K, d.M, d.lda, batch_maps, d.stride_a,
                                             atom_k, 128);
         const bool ok_b = mn_b ? encode_map(&plan->maps[1], d.dtype_b, B, d.N, d.K, d.ldb, batch_maps, d.stride_b,
-                                            64, info.tile_k)
+                                            (int)(128 / eb_b), info.tile_k)
                                : encode_map(&plan->maps[1], d.dtype_b, B, d.K, d.N, d.ldb, batch_maps, d.stride_b,
                                             atom_k, std::min(info.tile_n, 256) / cg);
         if (!ok_a || !ok_b ||
@@ -674,6 +676,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.mma_kind = d.dtype_a == GEMM_TF32 ? dgb::kMmaKindTF32 : dgb::kMmaKindF16;
     // A/B formats: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = tf32
     p.mn_major_a = d.major_a == GEMM_MN_MAJOR;
+    p.mn_box_elems = (int32_t)(128 / eb_a);
     p.mn_major_b = d.major_b == GEMM_MN_MAJOR;
     // one MMA covers at most 256 columns (512-wide tiles issue two)
     const uint32_t fmt = d.dtype_a == GEMM_BF16 ? 1u : (d.dtype_a == GEMM_TF32 ? 2u : 0u);
@@ -708,7 +711,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
         p.stride_sb = d.stride_sb;
         // kind::f8f6f4 formats: 0 = e4m3, 1 = e5m2
         p.idesc = dgb::make_idesc2(d.dtype_a == GEMM_E5M2 ? 1u : 0u, d.dtype_b == GEMM_E5M2 ? 1u : 0u,
-                                   (uint32_t)info.tile_m, (uint32_t)info.tile_n);
+                                   (uint32_t)info.tile_m, (uint32_t)info.tile_n, (uint32_t)p.mn_major_a,
+                                   (uint32_t)p.mn_major_b);
         e = dgb::launch_fp8_block(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
     } else {
         e = dgb::launch_persistent(p, cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);

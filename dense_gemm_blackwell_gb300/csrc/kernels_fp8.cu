@@ -134,12 +134,19 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                    const uint64_t da = smem_desc_sw128(sa);
-                    const uint64_t db = smem_desc_sw128(sa + p.stage_bytes_a);
+                    const uint32_t sb = sa + p.stage_bytes_a;
+                    // K-major: the next K32 is 32 bytes along the row (+2 in the
+                    // address field); MN-major: 32 k-rows of 128 B on (+256), atoms
+                    // along M/N one 16 KB box apart
+                    constexpr uint32_t kBox = 128u * kFp8TileK;
+                    const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
+                    const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
+                    const uint64_t step_a = p.mn_major_a ? 256u : 2u;
+                    const uint64_t step_b = p.mn_major_b ? 256u : 2u;
                     const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
 #pragma unroll
                     for (int kk = 0; kk < kFp8TileK / 32; ++kk)
-                        mma_f8<CG>(d_tmem, da + 2u * kk, db + 2u * kk, p.idesc, kk != 0);
+                        mma_f8<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc, kk != 0);
                     issued_any = true;
                     commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
                     if (++stage == S) { stage = 0; phase ^= 1u; }

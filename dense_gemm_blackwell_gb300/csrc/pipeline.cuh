@@ -126,18 +126,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // Copy one operand's slice for one ring stage: `rows` rows (M or N) of
 // `tile_k` K elements.  K-major: ATOMS boxes of (tile_k / ATOMS) x rows, one
 // 128-byte swizzle atom column each, `atom_stride` bytes apart (default
-// rows x 128 B).  MN-major (ATOMS == 1): boxes of 64 contiguous M/N elements
-// x tile_k k-rows, one per 64 rows, 8 KB apart.
+// rows x 128 B).  MN-major (ATOMS == 1): boxes of `mn_elems` contiguous M/N
+// elements (128 bytes) x tile_k k-rows, one per `mn_elems` rows, `mn_box_bytes`
+// apart.
 template <int CG, int ATOMS = 1>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, bool mn_major,
                                              int rows, int row0, int kx, int b, bool batched, bool hint,
-                                             uint64_t policy, int atom_k = 0, uint32_t atom_stride = 0) {
-    const int boxes = mn_major ? rows / 64 : ATOMS;
+                                             uint64_t policy, int atom_k = 0, uint32_t atom_stride = 0,
+                                             int mn_elems = 64, uint32_t mn_box_bytes = kMNMajorBoxBytes) {
+    const int boxes = mn_major ? rows / mn_elems : ATOMS;
     const uint32_t a_stride = atom_stride ? atom_stride : (uint32_t)rows * 128u;
     for (int j = 0; j < boxes; ++j) {
-        const int x = mn_major ? row0 + 64 * j : (ATOMS == 1 ? kx : kx + j * atom_k);
+        const int x = mn_major ? row0 + mn_elems * j : (ATOMS == 1 ? kx : kx + j * atom_k);
         const int y = mn_major ? kx : row0;
-        const uint32_t d = dst + (uint32_t)j * (mn_major ? kMNMajorBoxBytes : a_stride);
+        const uint32_t d = dst + (uint32_t)j * (mn_major ? mn_box_bytes : a_stride);
         if constexpr (CG == 1) {
             if (batched) {
                 if (hint) tma_load_3d_hint(d, map, bar, x, y, b, policy);
@@ -178,6 +180,8 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
     const uint32_t tx_bytes = (uint32_t)CG * stage_bytes;
     const int b_rows = p.tile_n / CG;
     const int atom_k = tile_k / ATOMS;
+    const int mn_elems = p.mn_box_elems > 0 ? p.mn_box_elems : 64;
+    const uint32_t mn_box_bytes = 128u * (uint32_t)tile_k;     // one MN-major box: tile_k rows of 128 B
     // Consecutive waves of a raster group reuse its A panels: keep them in L2.
     const bool keep_a = (p.l2_hints & kHintKeepA) != 0;
     const uint64_t pol_a = l2_policy_evict_last();
@@ -203,10 +207,10 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 const uint32_t sb = sa + p.stage_bytes_a;
                 const int kx = kb * tile_k;
                 load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
-                                        keep_a, pol_a, atom_k);
+                                        keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
                 if constexpr (HALVES == 1) {
                     load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
-                                            p.batched != 0, false, pol_a, atom_k);
+                                            p.batched != 0, false, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
                 } else {
                     constexpr int kHalfRows = 256 / CG;
 #pragma unroll

@@ -162,11 +162,17 @@ def test_mn_major_plans():
     # MN-major B is loaded in 64-column boxes: a pair's half tile must be a multiple of 64
     s, _ = query(M=8192, N=8192, K=8192, major_b=dg.GEMM_MN_MAJOR, flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=192)
     assert s == dg.GEMM_ERR_UNSUPPORTED
-    # tf32 needs K-major operands; the block-scaled kernel is K-major
+    # tf32 needs K-major operands
     s, _ = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_TF32, major_a=dg.GEMM_MN_MAJOR)
     assert s == dg.GEMM_ERR_UNSUPPORTED
-    s, _ = query(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, major_b=dg.GEMM_MN_MAJOR,
-                 scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    # block-scaled fp8: MN-major operands in 128-element boxes; a CTA's B rows
+    # must be a whole number of boxes (a 128-wide pair tile gives each CTA 64)
+    fp8 = dict(M=4096, N=4096, K=4096, dtype_a=dg.GEMM_E4M3, scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    for kw in (dict(major_a=dg.GEMM_MN_MAJOR), dict(major_b=dg.GEMM_MN_MAJOR),
+               dict(major_a=dg.GEMM_MN_MAJOR, major_b=dg.GEMM_MN_MAJOR, flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=256)):
+        s, info = query(**fp8, **kw)
+        assert s == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_FP8_BLOCK, kw
+    s, _ = query(**fp8, major_b=dg.GEMM_MN_MAJOR, flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=128)
     assert s == dg.GEMM_ERR_UNSUPPORTED
 
 

@@ -93,3 +93,37 @@ def test_fp8_full_size_sampled():
     got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
     r = compare(got, dref, s, "bf16", TOL_FP8)
     assert r["ok"], (r, info)
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("mn_a,mn_b", [(True, False), (False, True), (True, True)])
+def test_fp8_mn_major_bit_exact(cg_flag, mn_a, mn_b):
+    """fp8 reaches tcgen05 in either majorness (cuBLASDx "API Card: Blackwell
+    Pipeline (tcgen05)", precision and arrangement notes): an MN-major operand
+    is stored [k][m] (or [k][n]) and loaded as 128-element x 128-k boxes."""
+    prob = inputs.make("fp8_block8192", M=512, N=640, K=400, dist="ints", seed=35)
+    wl = prob.wl
+    A, B = prob.A, prob.B
+    if mn_a:
+        A = A.transpose(-1, -2).contiguous()
+    if mn_b:
+        B = B.transpose(-1, -2).contiguous()
+    D = torch.full((wl.M, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_F32,
+                        scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128, flags=cg_flag, tile_n=256,
+                        major_a=dg.GEMM_MN_MAJOR if mn_a else dg.GEMM_K_MAJOR,
+                        major_b=dg.GEMM_MN_MAJOR if mn_b else dg.GEMM_K_MAJOR)
+    with dg.Plan(desc) as plan:
+        plan.run(A.cuda(), B.cuda(), D, prob.scale_a.cuda(), prob.scale_b.cuda())
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, (dg.gemm_status_string(s), rec.role)
+        info = plan.info.as_dict()
+    assert info["kernel"] == dg.GEMM_KERNEL_FP8_BLOCK
+    dref, sabs = oracle.gemm(A, B, M=wl.M, N=wl.N, K=wl.K, dtype_a="e4m3", dtype_b="e4m3",
+                             major_a="mn" if mn_a else "k", major_b="mn" if mn_b else "k",
+                             scale_a=prob.scale_a.numpy(), scale_b=prob.scale_b.numpy())
+    got = D.double().cpu().numpy()
+    r = compare(got, dref[0], sabs[0], "f32", TOL_FP8, exact=True)
+    if not r["ok"]:
+        dump_on_failure("fp8_mn_%d%d_cg%d" % (mn_a, mn_b, info["cta_group"]), got=got, dref=dref[0], sabs=sabs[0])
+    assert r["ok"], (r, info)
