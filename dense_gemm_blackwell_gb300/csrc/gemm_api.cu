@@ -494,6 +494,32 @@ gemm_status_t noalloc_address(int dev, void** out) {
 
 }  // namespace
 
+constexpr int kHostPanels = 8;    // gemm_run_host: at most this many row (or batch) panels
+constexpr int kHostJobs = kHostPanels + 1;
+
+// One GEMM of gemm_run_host's pipeline: rows (or batch entries) [u0, u0+nu)
+// of A and D against rows [n0, n0+nn) of B (all of B for batch panels, which
+// take their own entries of B).  Before it, the copy-in stream brings that
+// many rows of A (unless the previous job of the same panel did) and the
+// given range of B.
+struct HostJob {
+    int64_t u0, nu, n0, nn;
+    bool copy_a;
+    int64_t b0, bn;                   // rows of B (row panels) to copy before this job; bn = 0: none
+    struct gemm_plan_s* sub;
+};
+
+// gemm_run_host's pipeline: copy streams, events and one data-parallel plan
+// per job (sharing the parent's status record), created on first use.
+struct HostPipe {
+    bool ready = false;
+    int jobs = 0;
+    HostJob job[kHostJobs] = {};
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[kHostJobs] = {}, ev_g[kHostJobs] = {};
+};
+
 struct gemm_plan_s {
     CUtensorMap maps[3];          // A, B, D tensor maps of the last pointers seen
     const void* map_ptrs[3];
@@ -506,7 +532,22 @@ struct gemm_plan_s {
     uint32_t* sk_flags;
     float* sk_partials;
     uint32_t epoch;               // launches so far (stream-K flags carry the launch's value)
+    HostPipe* pipe = nullptr;     // gemm_run_host's panels (owned; sub-plans share `status`)
 };
+
+static void host_pipe_free(HostPipe* hp) {
+    if (!hp) return;
+    for (int i = 0; i < kHostJobs; ++i) {
+        if (hp->ev_a[i]) cudaEventDestroy(hp->ev_a[i]);
+        if (hp->ev_g[i]) cudaEventDestroy(hp->ev_g[i]);
+        delete hp->job[i].sub;
+    }
+    if (hp->ev_start) cudaEventDestroy(hp->ev_start);
+    if (hp->ev_done) cudaEventDestroy(hp->ev_done);
+    if (hp->h2d) cudaStreamDestroy(hp->h2d);
+    if (hp->d2h) cudaStreamDestroy(hp->d2h);
+    delete hp;
+}
 
 extern "C" {
 
@@ -720,6 +761,86 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
+// Panels for gemm_run_host: rows of A and D (one batch entry), or batch
+// entries; each panel large enough that its GEMM keeps the GPU busy.
+static int host_panels(const gemm_desc_t& d, int64_t* unit0) {
+    const int64_t units = d.batch > 1 ? d.batch : d.M;
+    int64_t want = d.batch > 1 ? d.batch / 64 : d.M / 1024;
+    if (want > kHostPanels) want = kHostPanels;
+    if (want < 2 || d.K == 0) return 1;
+    const int64_t align = d.batch > 1 ? 1 : 256;          // whole pair-tile row bands
+    int n = 0;
+    unit0[0] = 0;
+    for (int i = 1; i <= want; ++i) {
+        int64_t u = std::min(units, round_up(ceil_div(units * i, want), align));
+        if (u > unit0[n]) unit0[++n] = u;
+    }
+    unit0[n] = units;
+    return n;
+}
+
+static gemm_status_t host_pipe_setup(gemm_plan_t plan) {
+    HostPipe* hp = new (std::nothrow) HostPipe();
+    if (!hp) return GEMM_ERR_RESOURCES;
+    cudaError_t e;
+    const gemm_desc_t& d = plan->desc;
+    int64_t unit0[kHostPanels + 1];
+    const int panels = host_panels(d, unit0);
+    auto fail = [&](cudaError_t err) { host_pipe_free(hp); return cuda_fail(err); };
+    if (panels > 1) {
+        const bool by_batch = d.batch > 1;
+        // Row panels: the first panel multiplies against the two halves of B's
+        // rows separately, so that its first half of D starts copying out once
+        // A's first rows and half of B are in, not all of B.
+        const int64_t ns = round_up(d.N / 2, 256);
+        const bool split = !by_batch && d.N >= 1024 && ns < d.N;
+        int n = 0;
+        for (int i = 0; i < panels; ++i) {
+            const int64_t u0 = unit0[i], nu = unit0[i + 1] - u0;
+            if (split && i == 0) {
+                hp->job[n++] = HostJob{u0, nu, 0, ns, true, 0, ns, nullptr};
+                hp->job[n++] = HostJob{u0, nu, ns, d.N - ns, false, ns, d.N - ns, nullptr};
+            } else {
+                hp->job[n++] = HostJob{u0, nu, 0, d.N, true, 0, (!by_batch && !split && i == 0) ? d.N : 0, nullptr};
+            }
+        }
+        hp->jobs = n;
+        if ((e = cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
+        if ((e = cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking)) != cudaSuccess) return fail(e);
+        if ((e = cudaEventCreateWithFlags(&hp->ev_start, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+        if ((e = cudaEventCreateWithFlags(&hp->ev_done, cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+        for (int i = 0; i < hp->jobs; ++i) {
+            HostJob& jb = hp->job[i];
+            if ((e = cudaEventCreateWithFlags(&hp->ev_a[i], cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+            if ((e = cudaEventCreateWithFlags(&hp->ev_g[i], cudaEventDisableTiming)) != cudaSuccess) return fail(e);
+            gemm_desc_t pd = d;
+            if (by_batch) pd.batch = jb.nu; else pd.M = jb.nu;
+            pd.N = jb.nn;
+            pd.flags |= GEMM_FLAG_NO_STREAM_K;       // no workspace: data-parallel tiles
+            Resolved r;
+            gemm_status_t s = resolve(&pd, &r);
+            gemm_plan_s* sp = s == GEMM_OK ? new (std::nothrow) gemm_plan_s() : nullptr;
+            if (s == GEMM_OK && !sp) s = GEMM_ERR_RESOURCES;
+            if (s == GEMM_OK) {
+                jb.sub = sp;
+                sp->maps_valid = false;
+                sp->desc = r.d;
+                sp->props = plan->props;
+                sp->device = plan->device;
+                sp->status = plan->status;           // shared: gemm_sync_status sees every job
+                s = ::plan(r.d, plan->props, &sp->info);
+            }
+            if (s == GEMM_OK) s = cap_resident(r.d, &sp->info);
+            if (s != GEMM_OK) { host_pipe_free(hp); return s; }
+            sp->info.stream_k_tiles = 0;
+            sp->info.workspace_bytes = 0;
+        }
+    }
+    hp->ready = true;
+    plan->pipe = hp;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, void* hD, const float* hsa,
                             const float* hsb, void* dA, void* dB, void* dD, float* dsa, float* dsb,
                             gemm_stream_t stream_) {
@@ -729,33 +850,137 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, vo
     if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
     if (!hD || !dD) return GEMM_ERR_INVALID_ARG;
     const bool ka = d.major_a == GEMM_K_MAJOR, kb = d.major_b == GEMM_K_MAJOR;
-    // extent in elements of each operand: last element index + 1
-    const int64_t ext_a = (d.batch - 1) * d.stride_a + (ka ? (d.M - 1) * d.lda + d.K : (d.K - 1) * d.lda + d.M);
-    const int64_t ext_b = (d.batch - 1) * d.stride_b + (kb ? (d.N - 1) * d.ldb + d.K : (d.K - 1) * d.ldb + d.N);
-    const int64_t ext_d = (d.batch - 1) * d.stride_d + (d.M - 1) * d.ldd + d.N;
+    const bool scaled = d.scale_mode != GEMM_SCALE_NONE;
+    const int64_t eb_a = elem_bytes(d.dtype_a), eb_b = elem_bytes(d.dtype_b), eb_d = elem_bytes(d.dtype_d);
+    // extent in elements of one batch entry of each operand: last element index + 1
+    const int64_t one_a = ka ? (d.M - 1) * d.lda + d.K : (d.K - 1) * d.lda + d.M;
+    const int64_t one_b = kb ? (d.N - 1) * d.ldb + d.K : (d.K - 1) * d.ldb + d.N;
+    const int64_t one_d = (d.M - 1) * d.ldd + d.N;
+    const int64_t ext_b = (d.batch - 1) * d.stride_b + one_b;
+    const int64_t kblk = ceil_div(d.K, 128);
+    const int64_t one_sa = (d.M - 1) * d.ld_sa + kblk;
+    const int64_t ext_sb = (d.batch - 1) * d.stride_sb + (ceil_div(d.N, 128) - 1) * d.ld_sb + kblk;
     cudaError_t e;
     if (d.K > 0) {
         if (!hA || !hB || !dA || !dB) return GEMM_ERR_INVALID_ARG;
-        if ((e = cudaMemcpyAsync(dA, hA, (size_t)ext_a * elem_bytes(d.dtype_a), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-            return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(dB, hB, (size_t)ext_b * elem_bytes(d.dtype_b), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-            return cuda_fail(e);
-        if (d.scale_mode != GEMM_SCALE_NONE) {
-            if (!hsa || !hsb || !dsa || !dsb) return GEMM_ERR_INVALID_ARG;
-            const int64_t kblk = ceil_div(d.K, 128);
-            const int64_t ext_sa = (d.batch - 1) * d.stride_sa + (d.M - 1) * d.ld_sa + kblk;
-            const int64_t ext_sb = (d.batch - 1) * d.stride_sb + (ceil_div(d.N, 128) - 1) * d.ld_sb + kblk;
-            if ((e = cudaMemcpyAsync(dsa, hsa, (size_t)ext_sa * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-                return cuda_fail(e);
-            if ((e = cudaMemcpyAsync(dsb, hsb, (size_t)ext_sb * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-                return cuda_fail(e);
-        }
+        if (scaled && (!hsa || !hsb || !dsa || !dsb)) return GEMM_ERR_INVALID_ARG;
     }
-    gemm_status_t s = gemm_run(plan, dA, dB, dD, d.scale_mode != GEMM_SCALE_NONE ? dsa : nullptr,
-                               d.scale_mode != GEMM_SCALE_NONE ? dsb : nullptr, stream_);
-    if (s != GEMM_OK) return s;
-    if ((e = cudaMemcpyAsync(hD, dD, (size_t)ext_d * elem_bytes(d.dtype_d), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-        return cuda_fail(e);
+    if (!plan->pipe) {
+        gemm_status_t s = host_pipe_setup(plan);
+        if (s != GEMM_OK) return s;
+    }
+    HostPipe& hp = *plan->pipe;
+
+    if (hp.jobs == 0) {
+        // One piece: copy in, multiply, copy out, in stream order.
+        if (d.K > 0) {
+            const int64_t ext_a = (d.batch - 1) * d.stride_a + one_a;
+            if ((e = cudaMemcpyAsync(dA, hA, (size_t)(ext_a * eb_a), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                return cuda_fail(e);
+            if ((e = cudaMemcpyAsync(dB, hB, (size_t)(ext_b * eb_b), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                return cuda_fail(e);
+            if (scaled) {
+                const int64_t ext_sa = (d.batch - 1) * d.stride_sa + one_sa;
+                if ((e = cudaMemcpyAsync(dsa, hsa, (size_t)ext_sa * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                    return cuda_fail(e);
+                if ((e = cudaMemcpyAsync(dsb, hsb, (size_t)ext_sb * 4, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+                    return cuda_fail(e);
+            }
+        }
+        gemm_status_t s = gemm_run(plan, dA, dB, dD, scaled ? dsa : nullptr, scaled ? dsb : nullptr, stream_);
+        if (s != GEMM_OK) return s;
+        const int64_t ext_d = (d.batch - 1) * d.stride_d + one_d;
+        if ((e = cudaMemcpyAsync(hD, dD, (size_t)(ext_d * eb_d), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+            return cuda_fail(e);
+        return GEMM_OK;
+    }
+
+    // Jobs (row or batch-entry panels): the copy-in stream brings, ahead of
+    // each job, the rows of B and of A it is the first to need; the job's GEMM
+    // runs on `stream` once they landed, and its block of D goes back on the
+    // copy-out stream while later jobs still copy in or multiply.  Events keep
+    // the whole call ordered on `stream`.
+    const bool by_batch = d.batch > 1;
+    auto cu = [](const void* p, int64_t bytes) { return static_cast<const char*>(p) + bytes; };
+    auto mu = [](void* p, int64_t bytes) { return static_cast<char*>(p) + bytes; };
+    auto h2d = [&](void* dst, const void* src, int64_t bytes) {
+        return cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyHostToDevice, hp.h2d);
+    };
+    // rows [r0, r0+nr) of a row-per-M/N operand with leading dim ld (K-major) or
+    // columns of a [K][ld] operand (MN-major)
+    auto h2d_rows = [&](void* dbase, const void* hbase, bool kmaj, int64_t ld, int64_t eb, int64_t r0,
+                        int64_t nr) -> cudaError_t {
+        if (kmaj)
+            return cudaMemcpy2DAsync(mu(dbase, r0 * ld * eb), (size_t)(ld * eb), cu(hbase, r0 * ld * eb),
+                                     (size_t)(ld * eb), (size_t)(d.K * eb), (size_t)nr, cudaMemcpyHostToDevice,
+                                     hp.h2d);
+        return cudaMemcpy2DAsync(mu(dbase, r0 * eb), (size_t)(ld * eb), cu(hbase, r0 * eb), (size_t)(ld * eb),
+                                 (size_t)(nr * eb), (size_t)d.K, cudaMemcpyHostToDevice, hp.h2d);
+    };
+    const int64_t one_sb = (ceil_div(d.N, 128) - 1) * d.ld_sb + kblk;
+    if ((e = cudaEventRecord(hp.ev_start, stream)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(hp.h2d, hp.ev_start, 0)) != cudaSuccess) return cuda_fail(e);
+    for (int k = 0; k < hp.jobs; ++k) {
+        const HostJob& jb = hp.job[k];
+        int64_t off_a, off_b, off_d, off_sa, off_sb;   // element offsets of the job's operands
+        if (by_batch) {
+            off_a = jb.u0 * d.stride_a;
+            off_b = jb.u0 * d.stride_b;
+            off_d = jb.u0 * d.stride_d;
+            off_sa = jb.u0 * d.stride_sa;
+            off_sb = jb.u0 * d.stride_sb;
+            if ((e = h2d(mu(dA, off_a * eb_a), cu(hA, off_a * eb_a), ((jb.nu - 1) * d.stride_a + one_a) * eb_a)) !=
+                cudaSuccess)
+                return cuda_fail(e);
+            if ((e = h2d(mu(dB, off_b * eb_b), cu(hB, off_b * eb_b), ((jb.nu - 1) * d.stride_b + one_b) * eb_b)) !=
+                cudaSuccess)
+                return cuda_fail(e);
+            if (scaled) {
+                if ((e = h2d(dsa + off_sa, hsa + off_sa, ((jb.nu - 1) * d.stride_sa + one_sa) * 4)) != cudaSuccess)
+                    return cuda_fail(e);
+                if ((e = h2d(dsb + off_sb, hsb + off_sb, ((jb.nu - 1) * d.stride_sb + one_sb) * 4)) != cudaSuccess)
+                    return cuda_fail(e);
+            }
+        } else {
+            off_a = ka ? jb.u0 * d.lda : jb.u0;
+            off_b = kb ? jb.n0 * d.ldb : jb.n0;
+            off_d = jb.u0 * d.ldd + jb.n0;
+            off_sa = jb.u0 * d.ld_sa;
+            off_sb = (jb.n0 / 128) * d.ld_sb;
+            if (jb.bn > 0) {
+                if ((e = h2d_rows(dB, hB, kb, d.ldb, eb_b, jb.b0, jb.bn)) != cudaSuccess) return cuda_fail(e);
+                if (scaled) {
+                    const int64_t q0 = jb.b0 / 128, nq = ceil_div(jb.b0 + jb.bn, 128) - q0;
+                    if ((e = h2d(dsb + q0 * d.ld_sb, hsb + q0 * d.ld_sb, ((nq - 1) * d.ld_sb + kblk) * 4)) !=
+                        cudaSuccess)
+                        return cuda_fail(e);
+                }
+            }
+            if (jb.copy_a) {
+                if ((e = h2d_rows(dA, hA, ka, d.lda, eb_a, jb.u0, jb.nu)) != cudaSuccess) return cuda_fail(e);
+                if (scaled &&
+                    (e = h2d(dsa + off_sa, hsa + off_sa, ((jb.nu - 1) * d.ld_sa + kblk) * 4)) != cudaSuccess)
+                    return cuda_fail(e);
+            }
+        }
+        if ((e = cudaEventRecord(hp.ev_a[k], hp.h2d)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamWaitEvent(stream, hp.ev_a[k], 0)) != cudaSuccess) return cuda_fail(e);
+        gemm_status_t s = gemm_run(jb.sub, cu(dA, off_a * eb_a), cu(dB, off_b * eb_b), mu(dD, off_d * eb_d),
+                                   scaled ? dsa + off_sa : nullptr, scaled ? dsb + off_sb : nullptr, stream_);
+        if (s != GEMM_OK) return s;
+        if ((e = cudaEventRecord(hp.ev_g[k], stream)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamWaitEvent(hp.d2h, hp.ev_g[k], 0)) != cudaSuccess) return cuda_fail(e);
+        if (by_batch)
+            e = cudaMemcpyAsync(mu(hD, off_d * eb_d), cu(dD, off_d * eb_d), (size_t)(((jb.nu - 1) * d.stride_d + one_d) * eb_d),
+                                cudaMemcpyDeviceToHost, hp.d2h);
+        else
+            e = cudaMemcpy2DAsync(mu(hD, off_d * eb_d), (size_t)(d.ldd * eb_d), cu(dD, off_d * eb_d),
+                                  (size_t)(d.ldd * eb_d), (size_t)(jb.nn * eb_d), (size_t)jb.nu,
+                                  cudaMemcpyDeviceToHost, hp.d2h);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(hp.ev_done, hp.d2h)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(stream, hp.ev_done, 0)) != cudaSuccess) return cuda_fail(e);
     return GEMM_OK;
 }
 
@@ -819,6 +1044,7 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     if (!plan) return GEMM_OK;
     cudaError_t e = cudaSuccess;
+    host_pipe_free(plan->pipe);
     if (plan->status) e = cudaFree(plan->status);   // one allocation holds the workspace too
     delete plan;
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);

@@ -196,11 +196,22 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
 /*
  * gemm_run_host -- the same product for operands that live in host memory.
  * Copies hA, hB (and the scales) into the caller's device buffers dA, dB
- * (dsa, dsb), runs gemm_run into dD and copies dD back into hD, all enqueued
- * on `stream` with cudaMemcpyAsync (pinned host memory makes the copies
- * asynchronous).  Host and device buffers share the plan's layout (leading
- * dims and batch strides) and each must span that layout's extent.  The call
- * returns once the work is enqueued; synchronise `stream` before reading hD.
+ * (dsa, dsb), runs the product into dD and copies dD back into hD.  Host and
+ * device buffers share the plan's layout (leading dims and batch strides) and
+ * each must span that layout's extent; host memory should be pinned, or the
+ * copies are not asynchronous.
+ * Problems with at least 2048 rows (or 128 batch entries) are split into up
+ * to 8 row (or batch-entry) panels: B first, then each panel's rows of A are
+ * copied in on an internal stream while earlier panels multiply on `stream`
+ * and copy their rows of D out on a second internal stream (the first row
+ * panel is multiplied in two column halves, so its output starts leaving
+ * after half of B).  Events order everything after prior work on `stream`
+ * and before later work on it; the panels' GEMMs report device timeouts to
+ * the plan's record like gemm_run.  The internal streams, events and panel
+ * plans are created on the first call and freed by gemm_plan_destroy; calls
+ * on one plan must not run concurrently from several host threads.
+ * The call returns once the work is enqueued; synchronise `stream` before
+ * reading hD.
  */
 gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, void* hD,
                             const float* hscale_a, const float* hscale_b,
