@@ -4,29 +4,33 @@
 // stage count; cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", sections
 // "Depth and shared memory" and "Device side"):
 //
-//   warp 0, one lane  : TMA producer.  For every K slice of every tile it waits
-//                       for the ring slot to be empty, sets the expected bytes
-//                       on the slot's full barrier and issues two tensor copies
-//                       (A tile, B tile) that complete on it.
+//   warp 0, one lane  : TMA producer.  For every ring stage of every tile it
+//                       waits for the slot to be empty, sets the expected
+//                       bytes on the slot's full barrier and issues the A and
+//                       B tensor copies (one or two 128-byte K atoms each)
+//                       that complete on it.
 //   warp 1            : allocates tensor memory (whole warp); one lane of the
 //                       pair leader issues the MMAs: waits for a full slot,
-//                       issues four K16 tcgen05.mma (the tile's first starts a
-//                       fresh accumulator), commits to the slot's empty barrier;
-//                       after the tile's last slice commits to the
+//                       issues four K16 (K8 for tf32) tcgen05.mma per K atom
+//                       and accumulator half (the tile's first starts a fresh
+//                       accumulator), commits to the slot's empty barrier;
+//                       after the tile's last stage commits to the
 //                       accumulator's full barrier.
 //   warps 2..9        : epilogue.  Wait for a full accumulator, read it with
 //                       tcgen05.ld (one row per thread; two warps per 32-lane
-//                       quarter, each half of the columns), hand the buffer
-//                       back, convert, stage 32x128 B chunks in swizzled
+//                       quarter, sharing the chunks of each part), hand the
+//                       part back, convert, stage 32x128 B chunks in swizzled
 //                       shared memory and write D with TMA stores (coalesced
 //                       lines).
 //
-// Two accumulator buffers live in tensor memory, so the epilogue of tile t
-// overlaps the MMAs of tile t+1.  512-wide tiles (two N = 256 MMAs per K step)
-// fill all 512 columns with one accumulator: the MMAs of tile t+1 then wait
-// until every epilogue warp has loaded its last columns of tile t.  The grid is persistent: CTA (pair) c takes
-// tiles c, c+G, ... in a grouped raster that keeps a wave's A and B panels in L2.
-// Every thread follows the same tile sequence and leaves the loop together.
+// Tiles up to 256 wide keep two accumulators in tensor memory, so the
+// epilogue of tile t overlaps the MMAs of tile t+1.  512-wide tiles (two
+// N = 256 MMAs per K step) fill all 512 columns with one accumulator, handed
+// back in two 256-column halves: the MMAs of tile t+1 start on the left half
+// and wait for the right one after kWideLeadStages stages.  The grid is
+// persistent: CTA (pair) c takes tiles c, c+G, ... in a grouped raster that
+// keeps a wave's A and B panels in L2.  Every thread follows the same tile
+// sequence and leaves the loop together.
 //
 // cta_group::2: a cluster of two CTAs on neighbouring SMs computes a
 // (256 x tile_n) tile with one MMA stream issued by the even CTA.  Each CTA
@@ -34,7 +38,7 @@
 // shared memory; both CTAs' copies complete on the leader's full barrier.  The
 // leader's commits arrive on the empty / accumulator-full barriers of both
 // CTAs; each CTA's epilogue reads its own TMEM (its 128 rows) and both arrive on
-// the leader's accumulator-empty barrier.
+// the leader's accumulator-empty barriers.
 //
 // Every wait is bounded (wait_phase): on expiry the kernel records
 // GEMM_ERR_TIMEOUT, raises a CTA-wide abort flag, drains what it has in flight

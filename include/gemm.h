@@ -106,7 +106,9 @@ typedef struct {
     int64_t ld_sa, ld_sb;       /* scale leading dims in floats; 0 = ceil(K/128) */
     int64_t stride_sa, stride_sb;  /* floats between batch entries of the scales; 0 = packed */
     uint32_t flags;             /* GEMM_FLAG_* */
-    int32_t tile_n;             /* N extent of one MMA tile (multiple of 16, 16..256); 0 = planner */
+    int32_t tile_n;             /* N extent of one output tile: a multiple of 16 in 16..256, or 512 (16-bit/tf32
+                                   K-major operands: two N = 256 MMAs per K step, one 512-column accumulator);
+                                   block-scaled fp8: 128 or 256; 0 = planner */
     int32_t stages;             /* shared-memory ring depth (2..16); 0 = planner */
     int32_t max_ctas;           /* cap on persistent CTAs; 0 = all SMs */
     uint64_t wait_timeout_ns;   /* bound on every device-side wait; 0 = 2 s */
@@ -119,7 +121,7 @@ typedef struct {
     int32_t kernel;          /* gemm_kernel_t */
     int32_t cta_group;       /* 1 or 2 SMs per MMA */
     int32_t tile_m;          /* M extent of one MMA tile (128 per SM) */
-    int32_t tile_n;          /* N extent of one MMA tile */
+    int32_t tile_n;          /* N extent of one output tile (512: two N = 256 MMAs per K step) */
     int32_t tile_k;          /* K depth of one ring stage (64 for 16-bit, 128 for 8-bit inputs) */
     int32_t stages;          /* shared-memory ring depth */
     int32_t tmem_stages;     /* accumulator buffers in tensor memory */
