@@ -789,19 +789,44 @@ static gemm_status_t host_pipe_setup(gemm_plan_t plan) {
     auto fail = [&](cudaError_t err) { host_pipe_free(hp); return cuda_fail(err); };
     if (panels > 1) {
         const bool by_batch = d.batch > 1;
-        // Row panels: the first panel multiplies against the two halves of B's
-        // rows separately, so that its first half of D starts copying out once
-        // A's first rows and half of B are in, not all of B.
-        const int64_t ns = round_up(d.N / 2, 256);
-        const bool split = !by_batch && d.N >= 1024 && ns < d.N;
         int n = 0;
-        for (int i = 0; i < panels; ++i) {
-            const int64_t u0 = unit0[i], nu = unit0[i + 1] - u0;
-            if (split && i == 0) {
-                hp->job[n++] = HostJob{u0, nu, 0, ns, true, 0, ns, nullptr};
-                hp->job[n++] = HostJob{u0, nu, ns, d.N - ns, false, ns, d.N - ns, nullptr};
-            } else {
-                hp->job[n++] = HostJob{u0, nu, 0, d.N, true, 0, (!by_batch && !split && i == 0) ? d.N : 0, nullptr};
+        if (!by_batch && d.M >= 4096 && d.N >= 2048) {
+            // The copy-out is the long pole (D is the largest operand in and out
+            // of the GPU).  Keep it busy from early on: a first block of 40 % of
+            // A's rows, multiplied against B's four column quarters as each
+            // lands (while B streams in, each quarter yields a block of D about
+            // as large as the next quarter of B), then the remaining rows in
+            // panels against all of B.
+            const int64_t r0 = std::min(d.M, round_up(d.M * 2 / 5, 256));
+            int64_t q_prev = 0;
+            for (int q = 1; q <= 4; ++q) {
+                const int64_t qe = q == 4 ? d.N : std::min(d.N, round_up(ceil_div(d.N * q, 4), 256));
+                if (qe > q_prev) hp->job[n++] = HostJob{0, r0, q_prev, qe - q_prev, q_prev == 0, q_prev, qe - q_prev, nullptr};
+                q_prev = qe;
+            }
+            const int64_t rest = d.M - r0;
+            const int64_t np = std::min<int64_t>(kHostJobs - n, std::max<int64_t>(1, ceil_div(rest, 1024)));
+            int64_t u_prev = r0;
+            for (int64_t i = 1; i <= np && rest > 0; ++i) {
+                const int64_t ue = i == np ? d.M : std::min(d.M, r0 + round_up(ceil_div(rest * i, np), 256));
+                if (ue > u_prev) hp->job[n++] = HostJob{u_prev, ue - u_prev, 0, d.N, true, 0, 0, nullptr};
+                u_prev = ue;
+            }
+        } else {
+            // Row panels: the first panel multiplies against the two halves of B's
+            // rows separately, so that its first half of D starts copying out once
+            // A's first rows and half of B are in, not all of B.
+            const int64_t ns = round_up(d.N / 2, 256);
+            const bool split = !by_batch && d.N >= 1024 && ns < d.N;
+            for (int i = 0; i < panels; ++i) {
+                const int64_t u0 = unit0[i], nu = unit0[i + 1] - u0;
+                if (split && i == 0) {
+                    hp->job[n++] = HostJob{u0, nu, 0, ns, true, 0, ns, nullptr};
+                    hp->job[n++] = HostJob{u0, nu, ns, d.N - ns, false, ns, d.N - ns, nullptr};
+                } else {
+                    hp->job[n++] = HostJob{u0, nu, 0, d.N, true, 0, (!by_batch && !split && i == 0) ? d.N : 0,
+                                           nullptr};
+                }
             }
         }
         hp->jobs = n;

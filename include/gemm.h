@@ -203,11 +203,12 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
  * each must span that layout's extent; host memory should be pinned, or the
  * copies are not asynchronous.
  * Problems with at least 2048 rows (or 128 batch entries) are split into up
- * to 8 row (or batch-entry) panels: B first, then each panel's rows of A are
- * copied in on an internal stream while earlier panels multiply on `stream`
- * and copy their rows of D out on a second internal stream (the first row
- * panel is multiplied in two column halves, so its output starts leaving
- * after half of B).  Events order everything after prior work on `stream`
+ * to 9 GEMMs over row (or batch-entry) panels: operands are copied in on an
+ * internal stream while earlier GEMMs run on `stream` and copy their block of
+ * D out on a second internal stream.  With M >= 4096 and N >= 2048 a first
+ * block of 40 % of the rows is multiplied against B's four column quarters as
+ * they land, then the remaining rows in panels against all of B; otherwise the
+ * first row panel is multiplied in two column halves.  Events order everything after prior work on `stream`
  * and before later work on it; the panels' GEMMs report device timeouts to
  * the plan's record like gemm_run.  The internal streams, events and panel
  * plans are created on the first call and freed by gemm_plan_destroy; calls

@@ -93,3 +93,22 @@ def test_host_small_single_piece():
     prob = inputs.make("square8192_bf16", M=512, N=512, K=256, dist="ints", seed=95)
     got, dref, s = run_host(prob, "f32")
     assert compare(got, dref, s, "f32", TOL_16BIT, exact=True)["ok"]
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_host_first_block_quarters_bit_exact(out):
+    """M >= 4096 and N >= 2048: a first block of 40 % of the rows against B's
+    four column quarters, then the remaining rows in panels."""
+    prob = inputs.make("square8192_bf16", M=4352, N=2304, K=256, dist="ints", seed=96)
+    got, dref, s = run_host(prob, out)
+    r = compare(got, dref, s, out, TOL_16BIT, exact=True)
+    if not r["ok"]:
+        dump_on_failure("host_quarters_%s" % out, got=got, dref=dref, sabs=s)
+    assert r["ok"], r
+
+
+def test_host_first_block_quarters_block_scaled():
+    """The same schedule with fp8 operands: each quarter of B brings its rows of B's scales."""
+    prob = inputs.make("fp8_block8192", M=4096, N=2048, K=384, dist="ints", seed=97)
+    got, dref, s = run_host(prob, "bf16")
+    assert compare(got, dref, s, "bf16", TOL_FP8, exact=True)["ok"]
