@@ -112,48 +112,53 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     const uint64_t tmo = p.timeout_ns;
 
     if (warp == 0) {
-        if (lane == 0)
-            producer_loop<CG>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank, cluster_id,
-                              num_clusters);
+        producer_loop<CG>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank, cluster_id,
+                          num_clusters);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && leader) {
+        // The whole warp runs the loop and waits; one lane, elected once, issues
+        // every MMA and commit (a commit tracks only its own thread's MMAs).
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int pb = 0;
             bool aborted = false;
             bool issued_any = false;
+            const bool issuer = elect_one();
             for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     // completes once the block's bytes landed and its partial is free
-                    if (!wait_phase<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma, stage,
-                                           t)) {
+                    if (!wait_phase_warp<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma,
+                                                stage, t)) {
                         aborted = true;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                    const uint32_t sb = sa + p.stage_bytes_a;
-                    // K-major: the next K32 is 32 bytes along the row (+2 in the
-                    // address field); MN-major: 32 k-rows of 128 B on (+256), atoms
-                    // along M/N one 16 KB box apart
-                    constexpr uint32_t kBox = 128u * kFp8TileK;
-                    const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
-                    const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
-                    const uint64_t step_a = p.mn_major_a ? 256u : 2u;
-                    const uint64_t step_b = p.mn_major_b ? 256u : 2u;
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
+                    if (issuer) {
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                        const uint32_t sb = sa + p.stage_bytes_a;
+                        // K-major: the next K32 is 32 bytes along the row (+2 in the
+                        // address field); MN-major: 32 k-rows of 128 B on (+256), atoms
+                        // along M/N one 16 KB box apart
+                        constexpr uint32_t kBox = 128u * kFp8TileK;
+                        const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
+                        const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
+                        const uint64_t step_a = p.mn_major_a ? 256u : 2u;
+                        const uint64_t step_b = p.mn_major_b ? 256u : 2u;
+                        const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
 #pragma unroll
-                    for (int kk = 0; kk < kFp8TileK / 32; ++kk)
-                        mma_f8<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc, kk != 0);
-                    issued_any = true;
-                    commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
+                        for (int kk = 0; kk < kFp8TileK / 32; ++kk)
+                            mma_f8<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc, kk != 0);
+                        issued_any = true;
+                        commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
+                    }
+                    __syncwarp();
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                     if (++pb == PB) pb = 0;
                 }
             }
-            if (aborted && issued_any) {
+            if (aborted && issuer && issued_any) {
                 commit_local<CG>(drain_bar);
                 wait_phase_drain(drain_bar, 0, tmo);
             }

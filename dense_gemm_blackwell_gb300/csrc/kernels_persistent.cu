@@ -67,9 +67,11 @@ __host__ __device__ constexpr int batch_loads() { return OUT == GEMM_F32 ? 3 : 2
 // or K8 of tf32; ATOMS atoms per stage, rows x 128 B apart), commit the
 // stage back to the producer.  Per tile: wait for an empty accumulator
 // buffer first, commit it to the epilogue after the tile's last stage.
-// Issuing costs the thread about 45 cycles per MMA and 230 per barrier wait
-// (measured on GB300): at one atom per stage that is ~450 of the 512 cycles
-// the four MMAs of a 256 x 256 pair tile take, so the loop is kept lean.
+// Issuing costs about 45 cycles per MMA and, from a lone divergent lane, 230
+// per barrier wait (measured on GB300): at one atom per stage that is ~450 of
+// the 512 cycles the four MMAs of a 256 x 256 pair tile take.  So the whole
+// warp runs the loop and waits, and one lane, elected once, issues every MMA
+// and commit (a commit tracks only its own thread's MMAs).
 // HALVES = 2 (512-wide tiles): each K step is two N = 256 MMAs, into
 // accumulator columns [0, 256) and [256, 512), B rows of the second half
 // 256 / CG rows further on in the stage.  The two column halves are handed
@@ -94,17 +96,19 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
     uint32_t acc_phase = 0;
     bool aborted = false;
     bool issued_any = false;
+    const bool issuer = elect_one();
     WorkUnit u;
     for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
         const int t = u.tile;
-        if (!wait_phase<CG == 2>(tempty(acc, 0), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
+        if (!wait_phase_warp<CG == 2>(tempty(acc, 0), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc,
+                                      t)) {
             aborted = true;
             break;
         }
-        tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
-        // The MMAs of one ring stage for accumulator halves [h0, h1).
+        // The MMAs of one ring stage for accumulator halves [h0, h1); issuer lane only.
         auto issue_stage = [&](int st, int kb, int h0, int h1) {
+            tc_fence_after();
             const uint32_t sa = smem_u32(ring + (size_t)st * stage_bytes);
             const uint32_t sb = sa + p.stage_bytes_a;
             // K-major: next MMA's K is 32 bytes along the row (+2 in the
@@ -145,46 +149,55 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
             int st = stage;
             uint32_t ph = phase;
             for (int i = 0; i < lead; ++i) {
-                if (!wait_phase<false>(full(st), ph, abort_flag, tmo, p.status, kRoleMma, st, t)) {
+                if (!wait_phase_warp<false>(full(st), ph, abort_flag, tmo, p.status, kRoleMma, st, t)) {
                     aborted = true;
                     break;
                 }
-                tc_fence_after();
-                issue_stage(st, u.kb0 + i, 0, 1);
+                if (issuer) issue_stage(st, u.kb0 + i, 0, 1);
+                __syncwarp();
                 if (++st == S) { st = 0; ph ^= 1u; }
             }
             if (aborted) break;
-            if (!wait_phase<CG == 2>(tempty(acc, 1), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc, t)) {
+            if (!wait_phase_warp<CG == 2>(tempty(acc, 1), acc_phase ^ 1u, abort_flag, tmo, p.status, kRoleMma, acc,
+                                          t)) {
                 aborted = true;
                 break;
             }
-            tc_fence_after();
-            for (int i = 0; i < lead; ++i) {
-                issue_stage(stage, u.kb0 + i, 1, 2);
-                commit_to<CG>(empty(stage));
-                if (++stage == S) { stage = 0; phase ^= 1u; }
+            if (issuer) {
+                for (int i = 0, st2 = stage; i < lead; ++i) {
+                    issue_stage(st2, u.kb0 + i, 1, 2);
+                    commit_to<CG>(empty(st2));
+                    if (++st2 == S) st2 = 0;
+                }
             }
+            __syncwarp();
+            for (int i = 0; i < lead; ++i)
+                if (++stage == S) { stage = 0; phase ^= 1u; }
             kb = u.kb0 + lead;
         }
         for (; kb < u.kb1; ++kb) {
-            if (!wait_phase<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
+            if (!wait_phase_warp<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
                 aborted = true;
                 break;
             }
-            tc_fence_after();
-            issue_stage(stage, kb, 0, HALVES);
-            commit_to<CG>(empty(stage));
+            if (issuer) {
+                issue_stage(stage, kb, 0, HALVES);
+                commit_to<CG>(empty(stage));
+            }
+            __syncwarp();
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
-        commit_to<CG>(tfull(acc));
+        if (issuer) commit_to<CG>(tfull(acc));
+        __syncwarp();
         if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
     }
-    if (aborted && issued_any) {
+    if (aborted && issuer && issued_any) {
         // Abort: make sure every MMA issued so far has finished before TMEM is freed.
         commit_local<CG>(drain_bar);
         wait_phase_drain(drain_bar, 0, tmo);
     }
+    __syncwarp();
 }
 
 template <int CG, int OUT>
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        {
             if (p.tile_n > 256)
                 producer_loop<CG, 1, 2>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                         cluster_id, num_clusters);
@@ -268,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && leader) {
-            // the stage depth is a template argument: this thread is the
+        if (leader) {
+            // the stage depth is a template argument: this warp runs the
             // kernel's tightest loop, so no per-stage branching on it
             if (p.tile_n > 256)
                 mma_issuer<CG, 1, 2>(p, ring, stage_bytes, tmem_base, full0, empty0, tfull0, tempty0, drain_bar,

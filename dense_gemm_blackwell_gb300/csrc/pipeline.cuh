@@ -160,7 +160,8 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
     }
 }
 
-// TMA producer (one thread).  `tile_k` is the ring stage depth in elements of
+// TMA producer (one warp: every lane runs the loop and waits, one elected
+// lane issues).  `tile_k` is the ring stage depth in elements of
 // A/B: ATOMS 128-byte swizzle rows (one row: 64 for 16-bit, 128 for 8-bit
 // types).  HALVES = 2 for 512-wide tiles: B's tile rows are two 256-row
 // halves (one MMA each), every CTA loads its 256 / CG rows of each half; the
@@ -195,31 +196,35 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
             const uint32_t empty_bar = empty0 + 8u * stage;
             const uint32_t full_bar = full0 + 8u * stage;
-            if (!wait_phase<false>(empty_bar, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer, stage, t)) {
+            if (!wait_phase_warp<false>(empty_bar, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer, stage,
+                                        t)) {
                 aborted = true;
                 break;
             }
             const uint32_t fb = (CG == 2) ? map_to_cta(full_bar, 0) : full_bar;
-            if (leader) mbar_arrive_expect_tx(full_bar, tx_bytes);
             const bool drop = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0 && issued == 0;
-            if (!drop) {
-                const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                const uint32_t sb = sa + p.stage_bytes_a;
-                const int kx = kb * tile_k;
-                load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
-                                        keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
-                if constexpr (HALVES == 1) {
-                    load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
-                                            p.batched != 0, false, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
-                } else {
-                    constexpr int kHalfRows = 256 / CG;
+            if (elect_one()) {
+                if (leader) mbar_arrive_expect_tx(full_bar, tx_bytes);
+                if (!drop) {
+                    const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                    const uint32_t sb = sa + p.stage_bytes_a;
+                    const int kx = kb * tile_k;
+                    load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
+                                            keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
+                    if constexpr (HALVES == 1) {
+                        load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
+                                                p.batched != 0, false, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
+                    } else {
+                        constexpr int kHalfRows = 256 / CG;
 #pragma unroll
-                    for (int h = 0; h < HALVES; ++h)
-                        load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false, kHalfRows,
-                                                nb * p.tile_n + h * 256 + (int)rank * kHalfRows, kx, b,
-                                                p.batched != 0, false, pol_a, atom_k, (uint32_t)b_rows * 128u);
+                        for (int h = 0; h < HALVES; ++h)
+                            load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false, kHalfRows,
+                                                    nb * p.tile_n + h * 256 + (int)rank * kHalfRows, kx, b,
+                                                    p.batched != 0, false, pol_a, atom_k, (uint32_t)b_rows * 128u);
+                    }
                 }
             }
+            __syncwarp();
             ++issued;
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -228,8 +233,8 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
         // Tail: wait until the MMA released every slot, so that no commit
         // arrives on this CTA's barriers after it exits.
         for (int i = 0; i < S; ++i) {
-            if (!wait_phase<false>(empty0 + 8u * stage, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer,
-                                   stage, 0xFFFFFFFFu))
+            if (!wait_phase_warp<false>(empty0 + 8u * stage, phase ^ 1u, abort_flag, tmo, p.status,
+                                        kRoleProducer, stage, 0xFFFFFFFFu))
                 break;
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }

@@ -23,6 +23,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// One lane of the (fully active) warp is elected: true there, false elsewhere.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
