@@ -216,12 +216,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // one elected lane issue: on GB300 an MMA issue loop whose single divergent
 // lane also waits spends about 460 cycles per barrier wait and four MMAs,
 // against about 330 this way.
-template <bool kClusterScope>
+template <bool kClusterScope, bool kRelaxed = false>
 __device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                 uint64_t timeout_ns, gemm_device_error_t* st,
                                                 uint32_t role, uint32_t stage, uint32_t tile) {
     auto probe = [&]() {
-        return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+        if constexpr (kRelaxed) return mbar_try_wait_relaxed(bar, parity);
+        else return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     };
     if (__all_sync(0xffffffffu, probe())) return true;
     const uint64_t t0 = globaltimer_ns();

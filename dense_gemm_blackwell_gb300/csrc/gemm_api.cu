@@ -36,7 +36,7 @@ using dgb::SingleParams;
 
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-constexpr int kPersistentThreads = 320;   // producer, MMA and 8 epilogue warps
+constexpr int kPersistentThreads = 352;   // two producer warps, MMA warp and 8 epilogue warps
 constexpr int kSkFlagsPerCta = 8;         // stream-K: one published flag per epilogue warp
 constexpr int64_t kStagingBytes = 8 * 32 * 128;   // 8 epilogue warps x one 4 KB buffer
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B

@@ -4,13 +4,14 @@
 // stage count; cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", sections
 // "Depth and shared memory" and "Device side"):
 //
-//   warp 0, one lane  : TMA producer.  For every ring stage of every tile it
-//                       waits for the slot to be empty, sets the expected
-//                       bytes on the slot's full barrier and issues the A and
-//                       B tensor copies (one or two 128-byte K atoms each)
-//                       that complete on it.
-//   warp 1            : allocates tensor memory (whole warp); one lane of the
-//                       pair leader issues the MMAs: waits for a full slot,
+//   warps 0 and 10    : TMA producers.  For every ring stage of every tile
+//                       both wait for the slot to be empty; warp 0 sets the
+//                       expected bytes on the slot's full barrier and copies
+//                       A, warp 10 copies B (one or two 128-byte K atoms
+//                       each; for 512-wide tiles warp 0 also takes B's first
+//                       half), all completing on that barrier.
+//   warp 1            : allocates tensor memory (whole warp); the pair
+//                       leader's warp runs the MMA loop: waits for a full slot,
 //                       issues four K16 (K8 for tf32) tcgen05.mma per K atom
 //                       and accumulator half (the tile's first starts a fresh
 //                       accumulator), commits to the slot's empty barrier;
@@ -55,7 +56,8 @@ namespace dgb {
 
 constexpr uint32_t kStagingBytes = 32 * 128;  // one warp's output chunk: 32 rows x 128 B
 constexpr int kEpilogueWarps = 8;             // two per TMEM lane quarter, one half of the chunks each
-constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+constexpr int kThreads = 96 + 32 * kEpilogueWarps;   // + producer, MMA and second producer warps
+constexpr int kProducerBWarp = 2 + kEpilogueWarps;
 constexpr int kWideLeadStages = 2;            // 512-wide tiles: left-half stages issued before the right half is free
 // 32-column TMEM loads an epilogue warp holds in registers at once: as many as
 // fit the 168 registers a thread of a 10-warp CTA can have without spilling
@@ -265,18 +267,31 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     const int num_clusters = gridDim.x / CG;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        {
-            if (p.tile_n > 256)
-                producer_loop<CG, 1, 2>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
-                                        cluster_id, num_clusters);
-            else if (p.k_atoms == 2)
-                producer_loop<CG, 2, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
-                                        cluster_id, num_clusters);
+    if (warp == 0 || warp == kProducerBWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 0: A (+ B's first half of a 512-wide tile); the second producer: the rest of B
+        const bool first = warp == 0;
+        if (p.tile_n > 256) {
+            if (first)
+                producer_loop<CG, 1, 2, kPartA | kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag,
+                                                          rank, cluster_id, num_clusters);
             else
-                producer_loop<CG, 1, 1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
-                                        cluster_id, num_clusters);
+                producer_loop<CG, 1, 2, kPartB1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                                 cluster_id, num_clusters);
+        } else if (p.k_atoms == 2) {
+            if (first)
+                producer_loop<CG, 2, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                                cluster_id, num_clusters);
+            else
+                producer_loop<CG, 2, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                                 cluster_id, num_clusters);
+        } else {
+            if (first)
+                producer_loop<CG, 1, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                                cluster_id, num_clusters);
+            else
+                producer_loop<CG, 1, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                                 cluster_id, num_clusters);
         }
         __syncwarp();
     } else if (warp == 1) {

@@ -166,11 +166,22 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
 // types).  HALVES = 2 for 512-wide tiles: B's tile rows are two 256-row
 // halves (one MMA each), every CTA loads its 256 / CG rows of each half; the
 // stage holds B as [atom][half][rows of the half].  Like the MMA issuer, this
-// thread's loop is near its per-stage budget, so both are template arguments.
-template <int CG, int ATOMS = 1, int HALVES = 1>
+// warp's loop is near its per-stage budget, so both are template arguments.
+//
+// PARTS selects the copies this warp issues: kPartA (A, and the leader
+// CTA's expect_tx for the whole stage), kPartB0 (B, or B's first half),
+// kPartB1 (B's second half).  On GB300 a thread's TMA issue slows to about
+// 290 cycles a box when the SM's copies back up, so a 128 x 256 stage (two
+// boxes) issued by one warp takes longer than its 512 cycles of MMA; two
+// warps issuing A and B side by side each stay inside it.  Bytes of B may
+// land before A's warp posts the expect_tx: the barrier's pending arrival
+// keeps the phase open meanwhile (its tx-count may go below zero).
+constexpr uint32_t kPartA = 1u, kPartB0 = 2u, kPartB1 = 4u, kPartsAll = 7u;
+template <int CG, int ATOMS = 1, int HALVES = 1, uint32_t PARTS = kPartsAll>
 __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes, int tile_k,
                               uint32_t full0, uint32_t empty0, volatile uint32_t* abort_flag, uint32_t rank,
                               int cluster_id, int num_clusters) {
+    constexpr uint32_t parts = PARTS;
     const int S = p.stages;
     const bool leader = rank == 0;
     const uint64_t tmo = p.timeout_ns;
@@ -186,6 +197,9 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
     // Consecutive waves of a raster group reuse its A panels: keep them in L2.
     const bool keep_a = (p.l2_hints & kHintKeepA) != 0;
     const uint64_t pol_a = l2_policy_evict_last();
+    // pair: every CTA's copies complete on the leader's barrier
+    const uint32_t fb0 = (CG == 2) ? map_to_cta(full0, 0) : full0;
+    const bool drop_any = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0;
     WorkUnit u;
     for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
         const int t = u.tile;
@@ -194,33 +208,35 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
         const int a_row = mb * (128 * CG) + (int)rank * 128;
         const int b_row = nb * p.tile_n + (int)rank * b_rows;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-            const uint32_t empty_bar = empty0 + 8u * stage;
-            const uint32_t full_bar = full0 + 8u * stage;
-            if (!wait_phase_warp<false>(empty_bar, phase ^ 1u, abort_flag, tmo, p.status, kRoleProducer, stage,
-                                        t)) {
+            if (!wait_phase_warp<false, true>(empty0 + 8u * stage, phase ^ 1u, abort_flag, tmo, p.status,
+                                              kRoleProducer, stage, t)) {
                 aborted = true;
                 break;
             }
-            const uint32_t fb = (CG == 2) ? map_to_cta(full_bar, 0) : full_bar;
-            const bool drop = (p.flags & GEMM_FLAG_TEST_DROP_LOAD) && blockIdx.x == 0 && issued == 0;
+            const uint32_t fb = fb0 + 8u * stage;
+            const bool drop = drop_any && issued == 0;
             if (elect_one()) {
-                if (leader) mbar_arrive_expect_tx(full_bar, tx_bytes);
+                if (leader && (parts & kPartA) != 0) mbar_arrive_expect_tx(full0 + 8u * stage, tx_bytes);
                 if (!drop) {
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                     const uint32_t sb = sa + p.stage_bytes_a;
                     const int kx = kb * tile_k;
-                    load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b, p.batched != 0,
-                                            keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
+                    if constexpr ((parts & kPartA) != 0)
+                        load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b,
+                                                p.batched != 0, keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
                     if constexpr (HALVES == 1) {
-                        load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
-                                                p.batched != 0, false, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
+                        if constexpr ((parts & kPartB0) != 0)
+                            load_operand<CG, ATOMS>(sb, &p.tmap_b, fb, p.mn_major_b != 0, b_rows, b_row, kx, b,
+                                                    p.batched != 0, false, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
                     } else {
                         constexpr int kHalfRows = 256 / CG;
 #pragma unroll
                         for (int h = 0; h < HALVES; ++h)
-                            load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false, kHalfRows,
-                                                    nb * p.tile_n + h * 256 + (int)rank * kHalfRows, kx, b,
-                                                    p.batched != 0, false, pol_a, atom_k, (uint32_t)b_rows * 128u);
+                            if ((parts & (kPartB0 << h)) != 0)
+                                load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false,
+                                                        kHalfRows, nb * p.tile_n + h * 256 + (int)rank * kHalfRows,
+                                                        kx, b, p.batched != 0, false, pol_a, atom_k,
+                                                        (uint32_t)b_rows * 128u);
                     }
                 }
             }
@@ -238,8 +254,9 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 break;
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-    } else if (leader) {
-        // Abort: wait (bounded) for the copies still in flight into the ring.
+    } else if (leader && (parts & kPartA) != 0) {
+        // Abort: wait (bounded) for the copies still in flight into the ring
+        // (a stage's barrier counts the bytes of every warp's copies).
         int s = stage;
         uint32_t ph = phase;
         const int n = issued < S ? issued : S;

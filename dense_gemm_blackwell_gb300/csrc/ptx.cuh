@@ -100,6 +100,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // One probe of the phase with parity `parity` (true once that phase completed).
+// Relaxed form: no acquire ordering for this thread's later generic-proxy
+// accesses.  The TMA producer uses it on its empty barriers: what follows the
+// wait is only async-proxy copies, ordered after it by the control dependency.
+__device__ __forceinline__ bool mbar_try_wait_relaxed(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
