@@ -145,7 +145,7 @@ bool single_fits(const gemm_desc_t& d) {
 // Block-scaled e4m3: 256-column tiles (two 128-column halves, each one 128-row
 // block of B's scales), 128-deep K stages, two TMEM partial buffers of 256
 // columns, 8 promotion/epilogue warps with one 4 KB staging buffer each.
-constexpr int kFp8Threads = 320;
+constexpr int kFp8Threads = 384;
 constexpr int kFp8DefaultTileN = 256;           // planner default for block-scaled problems
 constexpr int kFp8DefaultCtaGroupNarrow = 2;    // pair form for 128-wide tiles
 constexpr int64_t kFp8StagingBytes = 8 * 32 * 128;

@@ -8,15 +8,19 @@
 // block-scaled MMA kinds (E8M0 scales per 32 elements) cannot express, so the
 // scales are applied in software, once per 128-deep K block:
 //
-//   warp 0, one lane : TMA producer (shared loop), one 128-deep K block per ring
-//                      stage (one 128-byte swizzle row of e4m3).
-//   warp 1           : allocates tensor memory; one lane of the pair leader
-//                      issues four K32 tcgen05.mma kind::f8f6f4 per block into a
+//   warps 0 and 2    : TMA producers (shared loop), one 128-deep K block per
+//                      ring stage (one 128-byte swizzle row of e4m3): warp 0
+//                      copies A and posts the stage's expected bytes, warp 2
+//                      copies B.
+//   warp 1           : allocates tensor memory; the pair leader's warp runs the
+//                      MMA loop, one elected lane issuing four K32 tcgen05.mma
+//                      kind::f8f6f4 per block into a
 //                      fresh partial P[j mod PB] (j counts blocks over all tiles)
 //                      and commits them to the stage's empty barrier.
-//   warps 2..9       : promotion and epilogue.  Warp w owns TMEM lanes
+//   warp 3           : idle.
+//   warps 4..11      : promotion and epilogue.  Warp w owns TMEM lanes
 //                      32*(w mod 4).. (its 32 rows) and 128 of the tile's 256
-//                      columns (half (w-2)/4, exactly one 128-row block of B).
+//                      columns (half (w-4)/4, exactly one 128-row block of B).
 //                      Per block: read its 32x128 slice of P with tcgen05.ld,
 //                      give the partial back, and accumulate
 //                      acc += P * (sA[row][kb] * sB[col/128][kb]) in registers.
@@ -25,6 +29,13 @@
 //
 // Two or four partial buffers let the tensor core compute block j+1 while the
 // epilogue warps promote block j.  Waits are bounded as in the 16-bit kernel.
+//
+// Registers: a promotion thread holds its row's 128 fp32 accumulators, and the
+// read-back of a partial is only fast with several tcgen05.ld in flight per
+// warp (one 16-column load at a time leaves the tensor core idle about half of
+// each block on GB300).  Twelve warps launch with 168 registers each; the first
+// warpgroup (producers, MMA) gives registers back (setmaxnreg) down to
+// kFp8RegsLow and the two promotion warpgroups take them up to kFp8RegsHigh.
 //
 // One barrier wait per block in the MMA thread.  In a thread with tcgen05.mma
 // in flight every mbarrier probe costs about 230 cycles (22 in a thread
@@ -47,9 +58,28 @@
 
 namespace dgb {
 
+// Move registers between the warpgroups of a CTA (every thread of the
+// warpgroup executes it).  The pool is what the CTA was launched with
+// (threads x registers per thread): an increase waits until other
+// warpgroups' decreases leave room, so callers keep the shares within it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 constexpr int kFp8TileK = 128;              // e4m3 elements per ring stage (128 B)
 constexpr int kFp8EpiWarps = 8;
-constexpr int kFp8Threads = 64 + 32 * kFp8EpiWarps;
+constexpr int kFp8EpiWarp0 = 4;                  // first promotion warp: warpgroups 1 and 2
+constexpr int kFp8Threads = 32 * (kFp8EpiWarp0 + kFp8EpiWarps);
+constexpr int kFp8LaunchRegs = 168;              // what 12 warps get: 3 per sub-partition's 16K registers
+constexpr int kFp8RegsLow = 72;                  // producers and MMA warpgroup
+constexpr int kFp8RegsHigh = 216;                // promotion warpgroups
+static_assert(128 * kFp8RegsLow + 32 * kFp8EpiWarps * kFp8RegsHigh <= kFp8Threads * kFp8LaunchRegs,
+              "register shares exceed the launch's pool");
 constexpr uint32_t kFp8StagingBytes = 32 * 128;   // one buffer per epilogue warp
 
 // COLS: columns of the tile each promotion warp owns (tile_n / 2): 128 for
@@ -111,67 +141,77 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     const int num_clusters = gridDim.x / CG;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        producer_loop<CG>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank, cluster_id,
-                          num_clusters);
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop and waits; one lane, elected once, issues
-        // every MMA and commit (a commit tracks only its own thread's MMAs).
-        if (leader) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int pb = 0;
-            bool aborted = false;
-            bool issued_any = false;
-            const bool issuer = elect_one();
-            for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    // completes once the block's bytes landed and its partial is free
-                    if (!wait_phase_warp<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma,
-                                                stage, t)) {
-                        aborted = true;
-                        break;
+    // Each role raises or lowers its registers first thing, so that the code
+    // that follows is compiled against its own share.
+    if (warp < kFp8EpiWarp0) {
+        setmaxnreg_dec<kFp8RegsLow>();
+        if (warp == 0) {
+            producer_loop<CG, 1, 1, kPartA>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank,
+                                            cluster_id, num_clusters);
+            __syncwarp();
+        } else if (warp == 2) {
+            producer_loop<CG, 1, 1, kPartB0>(p, ring, stage_bytes, kFp8TileK, full0, empty0, abort_flag, rank,
+                                             cluster_id, num_clusters);
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer
+            // The whole warp runs the loop and waits; one lane, elected once, issues
+            // every MMA and commit (a commit tracks only its own thread's MMAs).
+            if (leader) {
+                int stage = 0;
+                uint32_t phase = 0;
+                int pb = 0;
+                bool aborted = false;
+                bool issued_any = false;
+                const bool issuer = elect_one();
+                for (int t = cluster_id; t < p.num_tiles && !aborted; t += num_clusters) {
+                    for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                        // completes once the block's bytes landed and its partial is free
+                        if (!wait_phase_warp<false>(full0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleMma,
+                                                    stage, t)) {
+                            aborted = true;
+                            break;
+                        }
+                        if (issuer) {
+                            tc_fence_after();
+                            const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
+                            const uint32_t sb = sa + p.stage_bytes_a;
+                            // K-major: the next K32 is 32 bytes along the row (+2 in the
+                            // address field); MN-major: 32 k-rows of 128 B on (+256), atoms
+                            // along M/N one 16 KB box apart
+                            constexpr uint32_t kBox = 128u * kFp8TileK;
+                            const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
+                            const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
+                            const uint64_t step_a = p.mn_major_a ? 256u : 2u;
+                            const uint64_t step_b = p.mn_major_b ? 256u : 2u;
+                            const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
+    #pragma unroll
+                            for (int kk = 0; kk < kFp8TileK / 32; ++kk)
+                                mma_f8<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc, kk != 0);
+                            issued_any = true;
+                            commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
+                        }
+                        __syncwarp();
+                        if (++stage == S) { stage = 0; phase ^= 1u; }
+                        if (++pb == PB) pb = 0;
                     }
-                    if (issuer) {
-                        tc_fence_after();
-                        const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
-                        const uint32_t sb = sa + p.stage_bytes_a;
-                        // K-major: the next K32 is 32 bytes along the row (+2 in the
-                        // address field); MN-major: 32 k-rows of 128 B on (+256), atoms
-                        // along M/N one 16 KB box apart
-                        constexpr uint32_t kBox = 128u * kFp8TileK;
-                        const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
-                        const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
-                        const uint64_t step_a = p.mn_major_a ? 256u : 2u;
-                        const uint64_t step_b = p.mn_major_b ? 256u : 2u;
-                        const uint32_t d_tmem = tmem_base + (uint32_t)(pb * p.tile_n);
-#pragma unroll
-                        for (int kk = 0; kk < kFp8TileK / 32; ++kk)
-                            mma_f8<CG>(d_tmem, da + step_a * kk, db + step_b * kk, p.idesc, kk != 0);
-                        issued_any = true;
-                        commit_to<CG>(empty0 + 8u * stage);   // stage free, partial written
-                    }
-                    __syncwarp();
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                    if (++pb == PB) pb = 0;
+                }
+                if (aborted && issuer && issued_any) {
+                    commit_local<CG>(drain_bar);
+                    wait_phase_drain(drain_bar, 0, tmo);
                 }
             }
-            if (aborted && issuer && issued_any) {
-                commit_local<CG>(drain_bar);
-                wait_phase_drain(drain_bar, 0, tmo);
-            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        setmaxnreg_inc<kFp8RegsHigh>();
         // ------------------------------------------------------------ promotion + epilogue
         // D is written once and never read back here: let it leave L2 first.
         const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
         const uint64_t pol_d = l2_policy_evict_first();
         const int wq = warp & 3;                  // TMEM lane quarter
-        const int half = (warp - 2) >> 2;         // which COLS columns of the tile
-        uint8_t* buf = staging + (warp - 2) * kFp8StagingBytes;
+        const int half = (warp - kFp8EpiWarp0) >> 2;   // which COLS columns of the tile
+        uint8_t* buf = staging + (warp - kFp8EpiWarp0) * kFp8StagingBytes;
         int pb = 0;
         int stage = 0;
         uint32_t phase = 0;
@@ -238,17 +278,20 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                             acc[48 + i] = fmaf(__uint_as_float(r3[i]), s, acc[48 + i]);
                         }
                     } else {
-                        // 16-column loads keep the register footprint within what a
-                        // 10-warp CTA can hold (3 warps share a sub-partition's 16K registers).
+                        // two 16-column loads in flight, one wait per pair
 #pragma unroll
-                        for (int c = 0; c < COLS / 16; ++c) {
-                            uint32_t r[16];
-                            tmem_ld_32x32b_x16(taddr + c * 16, r);
+                        for (int c = 0; c < COLS / 16; c += 2) {
+                            uint32_t r0[16], r1[16];
+                            tmem_ld_32x32b_x16(taddr + c * 16, r0);
+                            tmem_ld_32x32b_x16(taddr + c * 16 + 16, r1);
                             tmem_wait_ld();
-                            tmem_reg_fence16(r);
+                            tmem_reg_fence16(r0);
+                            tmem_reg_fence16(r1);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), s, acc[c * 16 + i]);
+                            for (int i = 0; i < 16; ++i) {
+                                acc[c * 16 + i] = fmaf(__uint_as_float(r0[i]), s, acc[c * 16 + i]);
+                                acc[c * 16 + 16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[c * 16 + 16 + i]);
+                            }
                         }
                     }
                 }
@@ -340,9 +383,20 @@ static cudaLaunchConfig_t fp8_config(size_t smem, int grid, cudaStream_t stream,
     return cfg;
 }
 
+// The kernel's setmaxnreg shares assume it was built with kFp8LaunchRegs
+// registers per thread: with fewer the promotion warps' increase could never
+// be granted, so such a build is refused rather than launched.
+template <typename Kern>
+static bool fp8_regs_ok(Kern kern) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kern) != cudaSuccess) return false;
+    return a.numRegs == kFp8LaunchRegs;
+}
+
 template <int CG, int OUT, int COLS>
 static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = fp8_block_kernel<CG, OUT, COLS>;
+    if (!fp8_regs_ok(kern)) return cudaErrorInvalidConfiguration;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
@@ -354,6 +408,7 @@ static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t 
 template <int CG, int OUT, int COLS>
 static int fp8_clusters_typed(size_t smem) {
     auto kern = fp8_block_kernel<CG, OUT, COLS>;
+    if (!fp8_regs_ok(kern)) return 0;
     static std::atomic<int> smem_set[kMaxDevices];
     if (ensure_smem_limit(kern, smem, smem_set) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];

@@ -196,7 +196,7 @@ def test_fp8_block_plan():
     assert s == dg.GEMM_OK
     assert info.kernel == dg.GEMM_KERNEL_FP8_BLOCK
     assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (1, 128, 256, 128)
-    assert info.block_threads == 320 and info.tmem_cols == 512
+    assert info.block_threads == 384 and info.tmem_cols == 512
     assert info.smem_bytes <= GB300.smem_optin_bytes and info.stages >= 4
     # e4m3 requires block scales; 16-bit inputs refuse them
     s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3)
