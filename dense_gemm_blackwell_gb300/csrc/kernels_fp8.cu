@@ -91,6 +91,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     constexpr int kOutBytes = (OUT == GEMM_F32) ? 4 : 2;
     constexpr int kChunkCols = 128 / kOutBytes;          // columns per 128-byte staging row
     constexpr int kChunks = COLS / kChunkCols;           // chunks per warp's columns
+    // hand a partial back before the last FMAs (with 128 columns per warp the
+    // compiler then spills)
+    constexpr bool kEarlyRelease = COLS == 64;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -249,58 +252,43 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                 sb0 = sb1;
                 sa1 = (scaled && kb + 2 < nkb) ? __ldg(sa_row + kb + 2) : 0.0f;
                 sb1 = (scaled && kb + 2 < nkb) ? __ldg(sb_blk + kb + 2) : 0.0f;
-                int ok = 0;
-                if (lane == 0)
-                    ok = wait_phase<false>(empty0 + 8u * stage, phase, abort_flag, tmo, p.status, kRoleEpilogue,
-                                           stage, t);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                const bool ok = wait_phase_warp<false>(empty0 + 8u * stage, phase, abort_flag, tmo, p.status,
+                                                       kRoleEpilogue, stage, t);
                 if (!ok) { aborted = true; break; }
                 tc_fence_after();
+                // partial pb is free again once this warp's last tcgen05.ld of it
+                // completed: count towards block j + PB's full barrier (64-column
+                // warps before their last FMAs, which block j + PB need not wait for)
                 if (cols_ok) {
                     const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(pb * p.tile_n + half * COLS);
-                    if constexpr (COLS == 64) {
-                        // all four 16-column loads in flight, one wait
-                        uint32_t r0[16], r1[16], r2[16], r3[16];
-                        tmem_ld_32x32b_x16(taddr, r0);
-                        tmem_ld_32x32b_x16(taddr + 16, r1);
-                        tmem_ld_32x32b_x16(taddr + 32, r2);
-                        tmem_ld_32x32b_x16(taddr + 48, r3);
+                    // two 16-column loads in flight, one wait per pair: on GB300
+                    // faster than four in flight
+#pragma unroll
+                    for (int c = 0; c < COLS / 16; c += 2) {
+                        uint32_t r0[16], r1[16];
+                        tmem_ld_32x32b_x16(taddr + c * 16, r0);
+                        tmem_ld_32x32b_x16(taddr + c * 16 + 16, r1);
                         tmem_wait_ld();
                         tmem_reg_fence16(r0);
                         tmem_reg_fence16(r1);
-                        tmem_reg_fence16(r2);
-                        tmem_reg_fence16(r3);
+                        if (kEarlyRelease && c + 2 == COLS / 16) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0 && left > PB)
+                                arrive_leader<CG>(full0 + 8u * (stage + PB < S ? stage + PB : stage + PB - S));
+                        }
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            acc[i] = fmaf(__uint_as_float(r0[i]), s, acc[i]);
-                            acc[16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[16 + i]);
-                            acc[32 + i] = fmaf(__uint_as_float(r2[i]), s, acc[32 + i]);
-                            acc[48 + i] = fmaf(__uint_as_float(r3[i]), s, acc[48 + i]);
-                        }
-                    } else {
-                        // two 16-column loads in flight, one wait per pair
-#pragma unroll
-                        for (int c = 0; c < COLS / 16; c += 2) {
-                            uint32_t r0[16], r1[16];
-                            tmem_ld_32x32b_x16(taddr + c * 16, r0);
-                            tmem_ld_32x32b_x16(taddr + c * 16 + 16, r1);
-                            tmem_wait_ld();
-                            tmem_reg_fence16(r0);
-                            tmem_reg_fence16(r1);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                acc[c * 16 + i] = fmaf(__uint_as_float(r0[i]), s, acc[c * 16 + i]);
-                                acc[c * 16 + 16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[c * 16 + 16 + i]);
-                            }
+                            acc[c * 16 + i] = fmaf(__uint_as_float(r0[i]), s, acc[c * 16 + i]);
+                            acc[c * 16 + 16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[c * 16 + 16 + i]);
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                // partial pb is free again: count towards block j + PB's full barrier
-                if (lane == 0 && left > PB) {
-                    const int rs = stage + PB < S ? stage + PB : stage + PB - S;
-                    arrive_leader<CG>(full0 + 8u * rs);
+                if (!kEarlyRelease || !cols_ok) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && left > PB)
+                        arrive_leader<CG>(full0 + 8u * (stage + PB < S ? stage + PB : stage + PB - S));
                 }
                 --left;
                 if (++pb == PB) pb = 0;

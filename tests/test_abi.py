@@ -195,9 +195,13 @@ def test_fp8_block_plan():
                     scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
     assert s == dg.GEMM_OK
     assert info.kernel == dg.GEMM_KERNEL_FP8_BLOCK
-    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (1, 128, 256, 128)
+    # SM pairs on 256x256 tiles when there are pair tiles for half the SMs
+    assert (info.cta_group, info.tile_m, info.tile_n, info.tile_k) == (2, 256, 256, 128)
     assert info.block_threads == 384 and info.tmem_cols == 512
     assert info.smem_bytes <= GB300.smem_optin_bytes and info.stages >= 4
+    s, info = query(M=128, N=8192, K=8192, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_BF16,
+                    scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128)
+    assert s == dg.GEMM_OK and (info.cta_group, info.tile_m, info.tile_n) == (1, 128, 256)
     # e4m3 requires block scales; 16-bit inputs refuse them
     s, _ = query(M=1024, N=1024, K=1024, dtype_a=dg.GEMM_E4M3)
     assert s == dg.GEMM_ERR_UNSUPPORTED
