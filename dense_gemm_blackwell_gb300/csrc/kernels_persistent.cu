@@ -341,10 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const int t = u.tile;
             int b, mb, nb;
             tile_coords(p, t, b, mb, nb);
-            int ok = 0;
-            if (lane == 0)
-                ok = wait_phase<false>(tfull(acc), acc_phase, abort_flag, tmo, p.status, kRoleEpilogue, acc, t);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const bool ok = wait_phase_warp<false>(tfull(acc), acc_phase, abort_flag, tmo, p.status, kRoleEpilogue,
+                                                   acc, t);
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
