@@ -59,8 +59,9 @@ def compare(d_gpu: np.ndarray, dref: np.ndarray, sabs: np.ndarray, out_dtype: st
 
 
 def dump_on_failure(name: str, **arrays) -> None:
-    """Save arrays of a failed comparison under gpurun_out/ (when that folder exists)."""
+    """Save arrays of a failed comparison into the folder named by $DGB_DUMP_DIR
+    (when set and existing), for offline inspection."""
     import os
-    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-    if os.path.isdir(out):
+    out = os.environ.get("DGB_DUMP_DIR", "")
+    if out and os.path.isdir(out):
         np.savez_compressed(os.path.join(out, "parity_fail_%s.npz" % name), **arrays)
