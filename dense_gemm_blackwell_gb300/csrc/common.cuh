@@ -118,19 +118,41 @@ struct PersistentParams {
     // Stream-K: the last sk_tiles tiles of the raster are split into equal K
     // ranges over all clusters and processed first.  A contributor (the part
     // of a tile that starts at K block 0) leaves its fp32 partial in
-    // sk_partials[slot] and publishes sk_flags = epoch; the finisher (the part
-    // that ends the tile) adds it before storing D.
+    // sk_partials[slot] and publishes sk_flags = the launch's epoch; the
+    // finisher (the part that ends the tile) adds it before storing D.
     int32_t sk_tiles;
-    uint32_t epoch;
     // Epilogue without shared-memory staging: each thread writes its row's
     // 128-byte chunks straight to D (frees the staging area for a ring stage).
     int32_t direct_store;
-    int32_t pad_;
     void* d_ptr;
     int64_t ldd, stride_d;
     float* sk_partials;       // [slot][cta rank][128 rows x tile_n], layout of sk_partial_index
     uint32_t* sk_flags;       // [slot][cta rank][8 epilogue warps]
+    // Launch counter in device memory, so that a launch replayed from a CUDA
+    // graph (same parameters) still gets a fresh epoch: [0] the epoch of the
+    // last launch that completed, [1] CTAs of the running launch that finished.
+    uint32_t* sk_epoch;
 };
+
+// The epoch of this launch: one past the last completed one (never 0, the
+// flags' initial value).  A CTA reads the same value whenever it asks before
+// its own finish, since the counter moves only once every CTA has finished.
+__device__ __forceinline__ uint32_t sk_launch_epoch(const uint32_t* sk_epoch) {
+    uint32_t last;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(last) : "l"(sk_epoch) : "memory");
+    return last + 1u == 0u ? 1u : last + 1u;
+}
+
+// Called by one thread of each CTA after all of its threads are done: the
+// last CTA to finish publishes the launch's epoch for the next launch.
+__device__ __forceinline__ void sk_finish_launch(uint32_t* sk_epoch, uint32_t epoch) {
+    __threadfence();
+    if (atomicAdd(sk_epoch + 1, 1u) == gridDim.x - 1) {
+        sk_epoch[1] = 0u;
+        sk_epoch[0] = epoch;
+        __threadfence();
+    }
+}
 
 constexpr uint32_t kHintKeepA = 1u;
 constexpr uint32_t kHintStreamD = 2u;

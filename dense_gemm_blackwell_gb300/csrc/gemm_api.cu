@@ -38,6 +38,10 @@ constexpr int kVersion = 10000;  // 1.0.0
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kPersistentThreads = 352;   // two producer warps, MMA warp and 8 epilogue warps
 constexpr int kSkFlagsPerCta = 8;         // stream-K: one published flag per epilogue warp
+// stream-K launch counter: two words in the plan's 256-byte status area, past
+// the error record (which gemm_sync_status clears) and zeroed with it at creation
+constexpr size_t kSkEpochOffset = 128;
+static_assert(sizeof(gemm_device_error_t) <= kSkEpochOffset, "error record overlaps the launch counter");
 constexpr int64_t kStagingBytes = 8 * 32 * 128;   // 8 epilogue warps x one 4 KB buffer
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
 constexpr int kDefaultRasterGroup = 8;                 // m blocks per raster group (least DRAM traffic on GB300)
@@ -531,7 +535,6 @@ struct gemm_plan_s {
     gemm_device_error_t* status;  // device record; stream-K flags and partials follow it
     uint32_t* sk_flags;
     float* sk_partials;
-    uint32_t epoch;               // launches so far (stream-K flags carry the launch's value)
     HostPipe* pipe = nullptr;     // gemm_run_host's panels (owned; sub-plans share `status`)
 };
 
@@ -594,8 +597,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, const gemm_desc_t* desc) {
     p->status = nullptr;
     p->sk_flags = nullptr;
     p->sk_partials = nullptr;
-    p->epoch = 0;
-    // One allocation: status record (256 B), then stream-K flags, then partials.
+    // One allocation: status record and launch counter (256 B), then stream-K flags, then partials.
     const int64_t flag_bytes = info.stream_k_tiles
                                    ? round_up((int64_t)(info.grid / info.cta_group) * info.cta_group *
                                                   kSkFlagsPerCta * 4, 256) : 0;
@@ -738,9 +740,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.stride_d = d.stride_d;
     if (info.stream_k_tiles > 0 && plan->sk_flags != nullptr) {
         p.sk_tiles = info.stream_k_tiles;
-        p.epoch = ++plan->epoch;
-        if (p.epoch == 0) p.epoch = ++plan->epoch;   // 0 is the flags' initial value
         p.sk_flags = plan->sk_flags;
+        p.sk_epoch = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(plan->status) + kSkEpochOffset);
         p.sk_partials = plan->sk_partials;
     }
     if (info.kernel == GEMM_KERNEL_FP8_BLOCK) {

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 release_all();
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) store_release_gpu(flag, p.epoch);
+                if (lane == 0) store_release_gpu(flag, sk_launch_epoch(p.sk_epoch));
                 if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
                 continue;
             }
@@ -388,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             if (adds) {
                 int got = 0;
                 if (lane == 0)
-                    got = wait_flag(flag, p.epoch, abort_flag, tmo, p.status, kRoleEpilogue, u.slot, t);
+                    got = wait_flag(flag, sk_launch_epoch(p.sk_epoch), abort_flag, tmo, p.status, kRoleEpilogue,
+                                    u.slot, t);
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     release_all();
@@ -523,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, (uint32_t)p.tmem_cols);
     }
+    if (p.sk_tiles > 0 && threadIdx.x == 0) sk_finish_launch(p.sk_epoch, sk_launch_epoch(p.sk_epoch));
 }
 
 template <int CG, int OUT>

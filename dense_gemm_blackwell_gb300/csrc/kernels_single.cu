@@ -21,6 +21,7 @@
 #include "ptx.cuh"
 #include "common.cuh"
 #include "launch.h"
+#include "pipeline.cuh"
 
 namespace dgb {
 
@@ -35,20 +36,64 @@ __device__ __forceinline__ void store_out(void* D, int64_t idx, float v) {
     }
 }
 
-// Write 8 consecutive K elements of one operand row into its 128-byte swizzled
-// row: 16-byte chunk j of row r lands at chunk position j ^ (r mod 8).
-__device__ __forceinline__ void stage_chunk(uint8_t* block, int row, int j, const uint16_t* src,
-                                            int64_t row_stride, int64_t k_stride, int k0, int K,
-                                            bool row_ok) {
-    uint32_t w[4];
+// One 64-deep swizzle row block (K elements kbase .. kbase + 63) of an operand
+// row, zero past K or past the last row: chunk j (8 elements, 16 bytes) lands
+// at 16-byte position j ^ (row mod 8) of the row's 128 bytes.  A K-major row
+// whose block lies inside K takes eight 16-byte loads, all in flight before the
+// stores (rows start on 16-byte boundaries: leading dimensions are multiples of
+// 16 bytes); other rows go element by element.
+__device__ __forceinline__ void stage_row(uint8_t* block, int row, const uint16_t* src, int64_t row_stride,
+                                          int64_t k_stride, int kbase, int K, bool row_ok) {
+    uint8_t* dst = block + row * 128;
+    if (row_ok && k_stride == 1 && kbase + 64 <= K) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + row * row_stride + kbase);
+        uint4 v[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int k_lo = k0 + 2 * e, k_hi = k_lo + 1;
-        uint32_t lo = (row_ok && k_lo < K) ? src[row * row_stride + k_lo * k_stride] : 0u;
-        uint32_t hi = (row_ok && k_hi < K) ? src[row * row_stride + k_hi * k_stride] : 0u;
-        w[e] = lo | (hi << 16);
+        for (int j = 0; j < 8; ++j) v[j] = __ldg(s4 + j);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(dst + ((j ^ (row & 7)) << 4)) = v[j];
+        return;
     }
-    *reinterpret_cast<uint4*>(block + row * 128 + ((j ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k_lo = kbase + 8 * j + 2 * e, k_hi = k_lo + 1;
+            const uint32_t lo = (row_ok && k_lo < K) ? src[row * row_stride + k_lo * k_stride] : 0u;
+            const uint32_t hi = (row_ok && k_hi < K) ? src[row * row_stride + k_hi * k_stride] : 0u;
+            w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + ((j ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// 32 consecutive outputs of one row (columns col0 ..), 16 bytes per store when
+// all of them are in range (D's rows start on 16-byte boundaries and col0 is a
+// multiple of 32), element by element at the ragged right edge.
+template <int OUT>
+__device__ __forceinline__ void store_row32(void* D, int64_t base, int col0, int N, const uint32_t (&r)[32]) {
+    if (col0 + 32 <= N) {
+        if constexpr (OUT == GEMM_F32) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(D) + base + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dst[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(D) + base + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack2<OUT>(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]));
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < N) store_out<OUT>(D, base + col0 + i, __uint_as_float(r[i]));
+    }
 }
 
 template <int OUT>
@@ -84,11 +129,9 @@ __global__ void __launch_bounds__(128, 1) single_cta_kernel(const __grid_constan
     const int64_t a_rs = p.major_a == GEMM_K_MAJOR ? p.lda : 1, a_ks = p.major_a == GEMM_K_MAJOR ? 1 : p.lda;
     const int64_t b_rs = p.major_b == GEMM_K_MAJOR ? p.ldb : 1, b_ks = p.major_b == GEMM_K_MAJOR ? 1 : p.ldb;
     for (int kb = 0; kb < kblocks; ++kb) {
-        for (int j = 0; j < 8; ++j) {
-            stage_chunk(sa + kb * 128 * 128, tid, j, A, a_rs, a_ks, kb * 64 + j * 8, p.K, tid < p.M);
-            for (int r = tid; r < p.n_pad; r += 128)
-                stage_chunk(sb + kb * p.n_pad * 128, r, j, B, b_rs, b_ks, kb * 64 + j * 8, p.K, r < p.N);
-        }
+        stage_row(sa + kb * 128 * 128, tid, A, a_rs, a_ks, kb * 64, p.K, tid < p.M);
+        for (int r = tid; r < p.n_pad; r += 128)
+            stage_row(sb + kb * p.n_pad * 128, r, B, b_rs, b_ks, kb * 64, p.K, r < p.N);
     }
     // Generic-proxy writes -> async proxy (the tensor core), then publish to thread 0.
     fence_proxy_async_smem();
@@ -122,14 +165,7 @@ __global__ void __launch_bounds__(128, 1) single_cta_kernel(const __grid_constan
             tmem_ld_32x32b_x32(lane_base + c * 32, r);
             tmem_wait_ld();
             tmem_reg_fence(r);
-            if (row < p.M) {
-                const int64_t base = b * p.stride_d + (int64_t)row * p.ldd;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = c * 32 + i;
-                    if (col < p.N) store_out<OUT>(p.D, base + col, __uint_as_float(r[i]));
-                }
-            }
+            if (row < p.M) store_row32<OUT>(p.D, b * p.stride_d + (int64_t)row * p.ldd, c * 32, p.N, r);
         }
     }
     tc_fence_before();
