@@ -60,11 +60,12 @@ constexpr int kThreads = 96 + 32 * kEpilogueWarps;   // + producer, MMA and seco
 constexpr int kProducerBWarp = 2 + kEpilogueWarps;
 constexpr int kWideLeadStages = 2;            // 512-wide tiles: left-half stages issued before the right half is free
 // 32-column TMEM loads an epilogue warp holds in registers at once: as many as
-// fit the 168 registers a thread of a 10-warp CTA can have without spilling
+// fit the 168 registers a thread of an 11-warp CTA can have (3 warps share a
+// sub-partition's 16K registers) without spilling
 template <int OUT>
 __host__ __device__ constexpr int batch_loads() { return OUT == GEMM_F32 ? 3 : 2; }
 
-// MMA issuer (one thread of the pair leader).  Per ring stage: wait for the
+// MMA issuer (the pair leader's MMA warp).  Per ring stage: wait for the
 // stage's data, issue four MMAs per 128-byte K atom (K16 of 16-bit elements
 // or K8 of tf32; ATOMS atoms per stage, rows x 128 B apart), commit the
 // stage back to the producer.  Per tile: wait for an empty accumulator

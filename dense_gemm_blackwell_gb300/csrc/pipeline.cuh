@@ -2,10 +2,10 @@
 // producer loop, MMA commits and output packing.
 //
 // The producer follows the main loop of "Hopper and Blackwell GEMM" (warp
-// specialisation): one thread walks every K slice of every tile the CTA (pair)
-// owns, waits for the ring slot to be empty, announces the slot's expected
-// bytes on its full barrier and issues the A and B tensor copies that complete
-// on it.
+// specialisation): a producer warp walks every K slice of every tile the CTA
+// (pair) owns, waits for the ring slot to be empty, announces the slot's
+// expected bytes on its full barrier and issues tensor copies that complete on
+// it (a kernel may run two such warps, one for A and one for B).
 #pragma once
 
 #include <cuda_bf16.h>
