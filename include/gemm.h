@@ -188,7 +188,15 @@ gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info);
  * must be NULL otherwise.  A, B, D (and scales) must be 16-byte aligned and
  * every leading dimension / batch stride a multiple of 16 bytes
  * (GEMM_ERR_ALIGNMENT).  M, N or batch equal to 0 is a no-op; K equal to 0
- * writes zeros to D.  Tensor maps are encoded per call from the pointers.
+ * writes zeros to D.  Tensor maps are encoded on the host from the pointers
+ * (kept while the pointers stay the same).
+ * The call only enqueues kernels (no allocation, no synchronisation), so it
+ * may be captured into a CUDA graph and replayed: a plan whose tiles are
+ * split along K (stream-K, gemm_plan_info_t.stream_k_tiles > 0) takes each
+ * launch's epoch from a counter in its device memory, so replays stay
+ * correct.  Launches of one plan must be ordered (one stream, or streams
+ * joined by events): concurrent launches would share its status record,
+ * stream-K workspace and launch counter.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT or GEMM_ERR_CUDA.
  * Device-side wait expiry is not visible here; see gemm_sync_status.
  */
