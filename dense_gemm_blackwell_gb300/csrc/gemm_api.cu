@@ -45,6 +45,9 @@ static_assert(sizeof(gemm_device_error_t) <= kSkEpochOffset, "error record overl
 constexpr int64_t kStagingBytes = 8 * 32 * 128;   // 8 epilogue warps x one 4 KB buffer
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
 constexpr int kDefaultRasterGroup = 8;                 // m blocks per raster group (least DRAM traffic on GB300)
+// 512-wide tiles with at least 32 m blocks: groups of 16 read less from DRAM
+// (8192^3: 845 vs 869 MB per launch) and, under the power cap, run 0.6 % faster
+constexpr int kWideRasterGroup = 16;
 
 thread_local int g_last_cuda_error = 0;
 
@@ -712,7 +715,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     p.stages = info.stages;
     p.tmem_cols = info.tmem_cols;
     p.tmem_stages = info.tmem_stages;
-    p.group_m = d.raster_group > 0 ? d.raster_group : kDefaultRasterGroup;
+    p.group_m = d.raster_group > 0 ? d.raster_group
+                                   : (info.tile_n > 256 && p.num_m_blocks >= 2 * kWideRasterGroup ? kWideRasterGroup
+                                                                                                : kDefaultRasterGroup);
     p.batched = d.batch > 1 ? 1 : 0;
     p.tile_k = info.tile_k;
     p.k_atoms = (int32_t)(info.tile_k * eb_a / 128);   // 128-byte K atoms per stage
