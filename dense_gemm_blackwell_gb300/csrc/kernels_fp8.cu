@@ -139,6 +139,11 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the previous kernel of the stream; its results are
+    // visible from here on.  The next GEMM may be launched now: its CTAs take
+    // SMs as this grid's CTAs leave and wait in griddep_wait.
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int cluster_id = blockIdx.x / CG;
     const int num_clusters = gridDim.x / CG;
@@ -388,8 +393,11 @@ static cudaError_t fp8_launch_typed(const PersistentParams& p, int grid, size_t 
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = fp8_config<CG>(smem, grid, stream, attr);
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddep_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -263,6 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the previous kernel of the stream; its results are
+    // visible from here on.  The next GEMM may be launched now: its CTAs take
+    // SMs as this grid's CTAs leave and wait in griddep_wait.
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int cluster_id = blockIdx.x / CG;
     const int num_clusters = gridDim.x / CG;
@@ -539,13 +544,15 @@ static cudaError_t launch_typed(const PersistentParams& p, int grid, size_t smem
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddep_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

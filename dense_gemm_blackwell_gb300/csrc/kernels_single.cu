@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(128, 1) single_cta_kernel(const __grid_constan
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    // the previous kernel of the stream may still be running up to here
+    griddep_wait();
+    griddep_launch_dependents();
 
     // Stage A (row = tid) and B (rows tid, tid+128) into the swizzled layout.
     const uint16_t* A = static_cast<const uint16_t*>(p.A) + b * p.stride_a;
@@ -191,8 +194,17 @@ static cudaError_t launch_single_typed(const SingleParams& p, int batch, size_t 
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
-    kern<<<batch, 128, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)batch, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see griddep_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_single_cta(const SingleParams& p, int dtype_d, int batch, size_t smem_bytes,

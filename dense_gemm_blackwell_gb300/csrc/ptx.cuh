@@ -31,6 +31,15 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream is still
+// running: griddep_wait blocks until that kernel has completed and its memory
+// operations are visible (a no-op in an ordinary launch), so it precedes every
+// global-memory access; griddep_launch_dependents lets the next such launch
+// begin once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
