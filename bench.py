@@ -320,7 +320,11 @@ def run_ours(args):
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # The timed region holds only the K launches (consecutive launches on the
+    # stream overlap one kernel's set-up with the previous one's last CTAs,
+    # which an event recorded between them would prevent); the kernel's
+    # average launch duration is the region's time over K.  Per-launch
+    # durations come from a separate, shorter pass afterwards (reported only).
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -329,15 +333,20 @@ def run_ours(args):
     g1 = torch.cuda.Event(enable_timing=True)
     g0.record(stream)
     for i in range(args.steps):
-        events[i][0].record(stream)
         step()
-        events[i][1].record(stream)
     g1.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t_wall1 = time.time()
     total_ms = g0.elapsed_time(g1)
+    n_iso = min(args.steps, 50)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iso)]
+    for i in range(n_iso):
+        events[i][0].record(stream)
+        step()
+        events[i][1].record(stream)
+    torch.cuda.synchronize()
     launch_ms = [a.elapsed_time(b) for a, b in events]
     time.sleep(0.2)
     sampler.stop()
@@ -360,7 +369,7 @@ def run_ours(args):
 
     # roofline of the dominant (only) kernel, from its own launch events
     peak_bf16, peak_bf16_sustained, peak_kind = peaks()
-    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    mean_launch_ms = total_ms / args.steps
     if winfo["bound"] == "hbm":
         hbm, kind = hbm_peak()
         achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
@@ -389,7 +398,10 @@ def run_ours(args):
     hSA = prob.scale_a.pin_memory() if prob.scale_a is not None else None
     hSB = prob.scale_b.pin_memory() if prob.scale_b is not None else None
     hD = torch.empty(dshape, dtype=tdt[wl.dtype_out]).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
+    # 100 steps: host<->device copies on this platform now and then take
+    # 5-20 ms instead of about 2 (plain cudaMemcpyAsync of pinned buffers too),
+    # and a longer run keeps one such step from dominating the average
+    e2e_steps = max(3, min(args.steps, 100))
 
     def e2e_step():
         s = dg.gemm_run_host(plan.handle, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), ptr(hSA), ptr(hSB),
@@ -450,8 +462,9 @@ def run_ours(args):
                             "max": max(e2e_step_ms)}},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "launch_ms": {"mean": mean_launch_ms, "min": min(launch_ms), "max": max(launch_ms),
-                      "median": statistics.median(launch_ms)},
+        "launch_ms": {"mean_in_timed_region": mean_launch_ms,
+                      "separate_pass": {"launches": len(launch_ms), "min": min(launch_ms), "max": max(launch_ms),
+                                        "median": statistics.median(launch_ms)}},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
