@@ -71,6 +71,14 @@ __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// acc[0..1] += x[0..1] * s with one packed fp32 FMA (round to nearest, as two fmaf)
+__device__ __forceinline__ void fma2_rn(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
+    asm("{\n\t.reg .b64 a, x, s;\n\t"
+        "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+        "fma.rn.f32x2 a, x, s, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(x0), "r"(x1), "f"(s));
+}
+
 constexpr int kFp8TileK = 128;              // e4m3 elements per ring stage (128 B)
 constexpr int kFp8EpiWarps = 8;
 constexpr int kFp8EpiWarp0 = 4;                  // first promotion warp: warpgroups 1 and 2
@@ -283,9 +291,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
                                 arrive_leader<CG>(full0 + 8u * (stage + PB < S ? stage + PB : stage + PB - S));
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            acc[c * 16 + i] = fmaf(__uint_as_float(r0[i]), s, acc[c * 16 + i]);
-                            acc[c * 16 + 16 + i] = fmaf(__uint_as_float(r1[i]), s, acc[c * 16 + 16 + i]);
+                        for (int i = 0; i < 16; i += 2) {
+                            fma2_rn(acc[c * 16 + i], acc[c * 16 + i + 1], r0[i], r0[i + 1], s);
+                            fma2_rn(acc[c * 16 + 16 + i], acc[c * 16 + 17 + i], r1[i], r1[i + 1], s);
                         }
                     }
                 }
