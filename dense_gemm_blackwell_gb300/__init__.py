@@ -276,6 +276,17 @@ def make_desc(M, N, K, *, batch=1, dtype_a=GEMM_BF16, dtype_b=None, dtype_d=GEMM
     return d
 
 
+def current_stream_handle():
+    """cudaStream_t of torch's current stream on the current device.  Uses the
+    raw-handle query when this torch has it (torch.cuda.current_stream() builds
+    a Stream object, about 3 us per call)."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch._C._cuda_getDevice())
+    return torch.cuda.current_stream().cuda_stream
+
+
 class Plan:
     """A created plan (owns the C handle); use as a context manager or call close()."""
 
@@ -286,18 +297,17 @@ class Plan:
 
     def run(self, A, B, D, scale_a=None, scale_b=None, stream=None):
         """Enqueue on `stream` (default: torch's current stream); tensors are torch CUDA tensors."""
-        import torch
         if stream is None:
-            stream = torch.cuda.current_stream().cuda_stream
-        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
-        s = gemm_run(self.handle, ptr(A), ptr(B), ptr(D), ptr(scale_a), ptr(scale_b), stream)
+            stream = current_stream_handle()
+        s = lib().gemm_run(self.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(),
+                           None if scale_a is None else scale_a.data_ptr(),
+                           None if scale_b is None else scale_b.data_ptr(), stream)
         if s != GEMM_OK:
             raise GemmError(s, "gemm_run")
 
     def run_host(self, hA, hB, hD, dA, dB, dD, hsa=None, hsb=None, dsa=None, dsb=None, stream=None):
-        import torch
         if stream is None:
-            stream = torch.cuda.current_stream().cuda_stream
+            stream = current_stream_handle()
         ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
         s = gemm_run_host(self.handle, ptr(hA), ptr(hB), ptr(hD), ptr(hsa), ptr(hsb), ptr(dA), ptr(dB),
                           ptr(dD), ptr(dsa), ptr(dsb), stream)
@@ -305,9 +315,8 @@ class Plan:
             raise GemmError(s, "gemm_run_host")
 
     def sync_status(self, stream=None):
-        import torch
         if stream is None:
-            stream = torch.cuda.current_stream().cuda_stream
+            stream = current_stream_handle()
         return gemm_sync_status(self.handle, stream)
 
     def close(self):
