@@ -279,24 +279,24 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         const bool first = warp == 0;
         if (p.tile_n > 256) {
             if (first)
-                producer_loop<CG, 1, 2, kPartA | kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag,
+                producer_loop<CG, 1, 2, kPartA | kPartB0, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag,
                                                           rank, cluster_id, num_clusters);
             else
-                producer_loop<CG, 1, 2, kPartB1>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                producer_loop<CG, 1, 2, kPartB1, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                                  cluster_id, num_clusters);
         } else if (p.k_atoms == 2) {
             if (first)
-                producer_loop<CG, 2, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                producer_loop<CG, 2, 1, kPartA, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                                 cluster_id, num_clusters);
             else
-                producer_loop<CG, 2, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                producer_loop<CG, 2, 1, kPartB0, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                                  cluster_id, num_clusters);
         } else {
             if (first)
-                producer_loop<CG, 1, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                producer_loop<CG, 1, 1, kPartA, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                                 cluster_id, num_clusters);
             else
-                producer_loop<CG, 1, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                producer_loop<CG, 1, 1, kPartB0, true>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
                                                  cluster_id, num_clusters);
         }
         __syncwarp();

@@ -177,7 +177,15 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
 // land before A's warp posts the expect_tx: the barrier's pending arrival
 // keeps the phase open meanwhile (its tx-count may go below zero).
 constexpr uint32_t kPartA = 1u, kPartB0 = 2u, kPartB1 = 4u, kPartsAll = 7u;
-template <int CG, int ATOMS = 1, int HALVES = 1, uint32_t PARTS = kPartsAll>
+//
+// kSerpentine: a cluster's odd-numbered whole tiles sweep K backwards.  The
+// clusters move through their tiles in step, one wave at a time, and a wave
+// touches more A and B (plus the D it writes) than L2 holds, so in a forward
+// sweep each wave finds its first K slices evicted.  Backwards, a wave starts
+// on the slices the previous one read last (8192^3 on GB300: 845 -> 694 MB
+// read from DRAM, 1.2 % faster at the power cap).  Only the summation order
+// of the tile changes; a kernel that applies per-K-block scales keeps it off.
+template <int CG, int ATOMS = 1, int HALVES = 1, uint32_t PARTS = kPartsAll, bool kSerpentine = false>
 __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t stage_bytes, int tile_k,
                               uint32_t full0, uint32_t empty0, volatile uint32_t* abort_flag, uint32_t rank,
                               int cluster_id, int num_clusters) {
@@ -220,7 +228,9 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                 if (!drop) {
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                     const uint32_t sb = sa + p.stage_bytes_a;
-                    const int kx = kb * tile_k;
+                    // the K block loaded: backwards on a cluster's odd whole tiles (kSerpentine)
+                    const bool back = kSerpentine && u.role == kUnitWhole && (idx & 1);
+                    const int kx = (back ? u.kb0 + u.kb1 - 1 - kb : kb) * tile_k;
                     if constexpr ((parts & kPartA) != 0)
                         load_operand<CG, ATOMS>(sa, &p.tmap_a, fb, p.mn_major_a != 0, 128, a_row, kx, b,
                                                 p.batched != 0, keep_a, pol_a, atom_k, 0, mn_elems, mn_box_bytes);
