@@ -333,6 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
         const int wq = warp & 3;                 // TMEM lanes [32*wq, 32*wq+32) are this warp's
         const int half = (warp - 2) >> 2;       // which of the lane quarter's two warps
         uint8_t* buf = staging + (warp - 2) * kStagingBytes;
+        // this warp's share of the operand ring, used by the last unit's stream-K fix-up
+        const uint32_t slice_bytes = ((uint32_t)S * stage_bytes / kEpilogueWarps) & ~15u;
+        const uint32_t slice = smem_u32(ring) + (uint32_t)(warp - 2) * slice_bytes;
+        const float4* slice_f4 = reinterpret_cast<const float4*>(ring + (size_t)(warp - 2) * slice_bytes);
         int acc = 0;
         uint32_t acc_phase = 0;
         const int nchunks = p.tile_n / kChunkCols;
@@ -368,21 +372,26 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 
             if (u.role == kUnitContributor) {
                 // Leave this K range's fp32 partial for the finisher, then publish it.
+                // Each accumulator part goes back to the MMA warp right after
+                // this warp's last TMEM load of it, before that load's stores.
                 float4* part = reinterpret_cast<float4*>(p.sk_partials) + part_base;
-                for (int c32 = 0; c32 < nchunks * kSub; ++c32) {
-                    const int c = c32 / kSub, cp = c % cpp;
-                    if ((cp < split) != (half == 0)) continue;     // the other warp's chunk
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_lane + c32 * 32, r);
-                    tmem_wait_ld();
-                    tmem_reg_fence(r);
+                for (int pt = 0; pt < parts; ++pt) {
+                    const int q_lo = (pt * cpp + (half == 0 ? 0 : split)) * kSub;   // this warp's 32-column loads
+                    const int q_hi = (pt * cpp + (half == 0 ? split : cpp)) * kSub;
+                    if (q_lo >= q_hi) release(pt);
+                    for (int q = q_lo; q < q_hi; ++q) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_lane + q * 32, r);
+                        tmem_wait_ld();
+                        tmem_reg_fence(r);
+                        if (q + 1 == q_hi) release(pt);
+                        float4* dst = part + sk_partial_index(p.tile_n, wq, q, 0, lane);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        part[sk_partial_index(p.tile_n, wq, c32, j, lane)] =
-                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        for (int j = 0; j < 8; ++j)
+                            dst[32 * j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    }
                 }
-                release_all();
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) store_release_gpu(flag, sk_launch_epoch(p.sk_epoch));
@@ -391,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             }
 
             const bool adds = u.role == kUnitFinisher;
+            bool staged = false;    // partial gathered into this warp's slice of the ring
             if (adds) {
                 int got = 0;
                 if (lane == 0)
@@ -404,6 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 uint32_t v;   // every lane acquires the flag before reading the partial
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
                 (void)v;
+                // A finisher is its cluster's last unit: with its accumulator
+                // full, no copy or MMA touches the operand ring again, so the
+                // partial is gathered there by asynchronous copies (a whole part
+                // in flight per thread) rather than by register loads.
+                WorkUnit nxt;
+                staged = (uint32_t)(split * kSub) * 4096u <= slice_bytes &&
+                         !next_unit(p, cluster_id, num_clusters, idx + 1, nxt);
+                if (staged) fence_proxy_async_smem();
             }
             const float4* part = reinterpret_cast<const float4*>(p.sk_partials) + part_base;
             // Chunks that hold at least one in-range column of an in-range row; the
@@ -413,6 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 const int c_lo = pt * cpp + (half == 0 ? 0 : split);          // this warp's chunks of the part
                 const int c_end = min(pt * cpp + (half == 0 ? split : cpp), n_valid);
                 if (c_lo >= c_end) release(pt);
+                if (staged) {
+                    // thread-private layout: this lane's float4 i of the part at i * 32 + lane
+                    for (int c = c_lo; c < c_end; ++c)
+                        for (int h = 0; h < kSub; ++h)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                cp_async_16(slice + (uint32_t)(((((c - c_lo) * kSub + h) * 8 + j) * 32 + lane) * 16),
+                                            part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                }
+                bool pending = staged;
                 const int first_nc = (c_end - c_lo) % kBatchChunks;
                 for (int c0 = c_lo; c0 < c_end;) {
                     const int nc = (c0 == c_lo && first_nc) ? first_nc : kBatchChunks;   // chunks in this batch
@@ -425,6 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     for (int q = 0; q < kBatchLoads; ++q)
                         if (q < nc * kSub) tmem_reg_fence(r[q]);
                     if (c0 + nc == c_end) release(pt);
+                    if (pending) {
+                        cp_async_wait_all();
+                        pending = false;
+                    }
                     if (p.acc_f16) {
                         // fp16 accumulator: the value is the low half of each 32-bit cell
 #pragma unroll
@@ -442,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                             for (int h = 0; h < kSub; ++h) {
 #pragma unroll
                                 for (int j = 0; j < 8; ++j) {
-                                    const float4 qv = __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                                    const float4 qv =
+                                        staged ? slice_f4[(((c - c_lo) * kSub + h) * 8 + j) * 32 + lane]
+                                               : __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
                                     // own part (later K) + partial (earlier K): one fixed order
                                     const int q = cc * kSub + h;
                                     r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);

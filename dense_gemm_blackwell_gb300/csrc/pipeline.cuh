@@ -49,9 +49,13 @@ constexpr int kUnitWhole = 0, kUnitContributor = 1, kUnitFinisher = 2;
 //     (finisher).  A cluster walks its range from the last segment to the
 //     first: it publishes its contributor partial before anything else and
 //     reaches its finisher segment last, when c-1's partial is long done.
-//  2. Data-parallel tiles c, c+G, ... of [0, T - sk_tiles).
+//  2. Data-parallel tiles c, c+G, ... of [0, T - sk_tiles).  Run after the
+//     stream-K region, they hide a finisher's fix-up behind the MMAs of the
+//     cluster's next tile; without them the finisher is the cluster's last
+//     unit and its fix-up the kernel's tail.
 __device__ __forceinline__ bool next_unit(const PersistentParams& p, int c, int G, int idx, WorkUnit& u) {
     const int nk = p.num_k_blocks;
+    const int dp_tiles = p.num_tiles - p.sk_tiles;
     if (p.sk_tiles > 0) {
         const int64_t total = (int64_t)p.sk_tiles * nk;
         const int64_t it0 = total * c / G;
@@ -61,7 +65,7 @@ __device__ __forceinline__ bool next_unit(const PersistentParams& p, int c, int 
             const int64_t j = (hi - 1) / nk;
             const int64_t lo = it0 > j * nk ? it0 : j * nk;
             if (k == idx) {
-                u.tile = p.num_tiles - p.sk_tiles + (int)j;
+                u.tile = dp_tiles + (int)j;
                 u.kb0 = (int)(lo - j * nk);
                 u.kb1 = (int)(hi - j * nk);
                 const bool starts = u.kb0 == 0, ends = u.kb1 == nk;
@@ -75,7 +79,7 @@ __device__ __forceinline__ bool next_unit(const PersistentParams& p, int c, int 
         idx -= k;
     }
     const int t = c + idx * G;
-    if (t >= p.num_tiles - p.sk_tiles) return false;
+    if (t >= dp_tiles) return false;
     u.tile = t;
     u.kb0 = 0;
     u.kb1 = nk;
