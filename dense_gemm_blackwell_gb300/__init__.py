@@ -19,7 +19,8 @@ __all__ = [
     "build", "lib", "GemmError", "GemmDesc", "GemmPlanInfo", "GemmDeviceProps", "GemmDeviceError",
     "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host", "gemm_run_noalloc",
     "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
-    "gemm_version", "gemm_schedule_model", "gemm_schedule_choose", "Plan", "matmul", "header_functions",
+    "gemm_version", "gemm_schedule_model", "gemm_schedule_choose", "gemm_plan_work_unit", "GemmWorkUnit", "Plan",
+    "matmul", "header_functions",
 ]
 
 # ---------------------------------------------------------------- constants (include/gemm.h)
@@ -69,6 +70,15 @@ class GemmPlanInfo(ctypes.Structure):
         ("pipeline_bytes", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
         ("stream_k_tiles", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
     ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemmWorkUnit(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("batch", ctypes.c_int32), ("m_block", ctypes.c_int32),
+                ("n_block", ctypes.c_int32), ("k_block_begin", ctypes.c_int32), ("k_block_end", ctypes.c_int32),
+                ("role", ctypes.c_int32), ("slot", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -131,6 +141,9 @@ def lib():
                 L.gemm_plan_create.restype = st
                 L.gemm_plan_info.argtypes = [vp, ctypes.POINTER(GemmPlanInfo)]
                 L.gemm_plan_info.restype = st
+                L.gemm_plan_work_unit.argtypes = [ctypes.POINTER(GemmDesc), ctypes.POINTER(GemmPlanInfo),
+                                                  ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(GemmWorkUnit)]
+                L.gemm_plan_work_unit.restype = st
                 L.gemm_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
                 L.gemm_run.restype = st
                 L.gemm_run_host.argtypes = [vp] * 12
@@ -184,6 +197,13 @@ def gemm_plan_info(plan) -> GemmPlanInfo:
     if s != GEMM_OK:
         raise GemmError(s, "gemm_plan_info")
     return info
+
+
+def gemm_plan_work_unit(desc: GemmDesc, info: GemmPlanInfo, cluster: int, index: int):
+    """(status, GemmWorkUnit): the index-th unit of a cluster of a persistent plan; tile -1 past its last."""
+    u = GemmWorkUnit()
+    s = lib().gemm_plan_work_unit(ctypes.byref(desc), ctypes.byref(info), cluster, index, ctypes.byref(u))
+    return s, u
 
 
 def gemm_run(plan, A, B, D, scale_a=None, scale_b=None, stream=None) -> int:

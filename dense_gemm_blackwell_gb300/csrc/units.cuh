@@ -1,0 +1,85 @@
+// units.cuh -- which output tile, and which K blocks of it, each cluster of a
+// persistent kernel works on, in order.  Host and device compile the same
+// functions: the kernels call them per unit, and gemm_plan_work_unit exposes
+// them to the host so that the schedule can be checked without a GPU.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace dgb {
+
+// Linear tile index -> (batch, m block, n block); tiles of one batch entry are
+// visited in groups of `group_m` m blocks, m fastest inside a group, so that
+// the CTAs of one wave share A and B panels and consecutive waves of a group
+// share its A panels in L2.
+__host__ __device__ __forceinline__ void tile_coords(const PersistentParams& p, int t, int& b, int& mb, int& nb) {
+    b = t / p.tiles_per_batch;
+    const int r = t - b * p.tiles_per_batch;
+    const int span = p.group_m * p.num_n_blocks;
+    const int g = r / span;
+    const int first_m = g * p.group_m;
+    const int gm = p.num_m_blocks - first_m < p.group_m ? p.num_m_blocks - first_m : p.group_m;
+    const int rr = r - g * span;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+// One piece of work of a cluster: K blocks [kb0, kb1) of one output tile.
+struct WorkUnit {
+    int tile;
+    int kb0, kb1;
+    int role;    // kUnitWhole, kUnitContributor or kUnitFinisher
+    int slot;    // partial slot written (contributor) or read (finisher)
+};
+constexpr int kUnitWhole = 0, kUnitContributor = 1, kUnitFinisher = 2;
+
+// The idx-th unit of cluster c (of G) in processing order.
+//  1. Stream-K region (tiles [T - sk_tiles, T)): its sk_tiles * nk K blocks
+//     are cut into G contiguous ranges, one per cluster.  Each range is at
+//     least one tile long (sk_tiles >= G), so a tile is split between at most
+//     two clusters: c-1 holds its start (contributor, slot c-1) and c its end
+//     (finisher).  A cluster walks its range from the last segment to the
+//     first: it publishes its contributor partial before anything else and
+//     reaches its finisher segment last, when c-1's partial is long done.
+//  2. Data-parallel tiles c, c+G, ... of [0, T - sk_tiles).  Run after the
+//     stream-K region, they hide a finisher's fix-up behind the MMAs of the
+//     cluster's next tile; without them the finisher is the cluster's last
+//     unit and its fix-up the kernel's tail.
+__host__ __device__ __forceinline__ bool next_unit(const PersistentParams& p, int c, int G, int idx, WorkUnit& u) {
+    const int nk = p.num_k_blocks;
+    const int dp_tiles = p.num_tiles - p.sk_tiles;
+    if (p.sk_tiles > 0) {
+        const int64_t total = (int64_t)p.sk_tiles * nk;
+        const int64_t it0 = total * c / G;
+        int64_t hi = total * (c + 1) / G;
+        int k = 0;
+        while (hi > it0) {
+            const int64_t j = (hi - 1) / nk;
+            const int64_t lo = it0 > j * nk ? it0 : j * nk;
+            if (k == idx) {
+                u.tile = dp_tiles + (int)j;
+                u.kb0 = (int)(lo - j * nk);
+                u.kb1 = (int)(hi - j * nk);
+                const bool starts = u.kb0 == 0, ends = u.kb1 == nk;
+                u.role = (starts && ends) ? kUnitWhole : (starts ? kUnitContributor : kUnitFinisher);
+                u.slot = starts ? c : c - 1;
+                return true;
+            }
+            ++k;
+            hi = lo;
+        }
+        idx -= k;
+    }
+    const int t = c + idx * G;
+    if (t >= dp_tiles) return false;
+    u.tile = t;
+    u.kb0 = 0;
+    u.kb1 = nk;
+    u.role = kUnitWhole;
+    u.slot = 0;
+    return true;
+}
+
+}  // namespace dgb

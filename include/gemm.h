@@ -181,6 +181,39 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, const gemm_desc_t* desc);
 /* gemm_plan_info -- copy the plan's decisions into *info. */
 gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info);
 
+/* One unit of a persistent kernel's work (see gemm_plan_work_unit). */
+typedef struct {
+    int32_t tile;            /* linear output tile, or -1: the cluster has no unit of that index */
+    int32_t batch;           /* the tile's batch entry */
+    int32_t m_block;         /* the tile covers D rows [m_block * tile_m, + tile_m) ... */
+    int32_t n_block;         /* ... and columns [n_block * tile_n, + tile_n), clipped to M and N */
+    int32_t k_block_begin;   /* contraction range [k_block_begin * tile_k, k_block_end * tile_k), */
+    int32_t k_block_end;     /* clipped to K */
+    int32_t role;            /* 0 whole tile; 1 stream-K contributor (leaves an fp32 partial);
+                                2 stream-K finisher (adds that partial and writes D) */
+    int32_t slot;            /* partial slot written (role 1) or read (role 2); 0 for role 0 */
+} gemm_work_unit_t;
+
+/*
+ * gemm_plan_work_unit -- the index-th unit (0-based, in processing order) of
+ * cluster `cluster` of a persistent plan; `desc` and `info` are the problem and
+ * its plan (gemm_plan_query or gemm_plan_info).  A cluster is info->cta_group
+ * CTAs sharing one MMA stream; there are info->grid / info->cta_group.  Host
+ * arithmetic only, touching no GPU: the same schedule functions the kernels
+ * run, compiled for the host, so a caller can check which tiles and K ranges
+ * each SM (pair) takes.  Order: first the stream-K region's segments (the last
+ * wave plus one full wave, cut into equal K ranges, each cluster walking its
+ * range from the end), then data-parallel tiles, raster groups of m blocks
+ * first (the L2 reuse across a wave that the "Hopper and Blackwell GEMM" page
+ * asks for next to its table of ridges).  The block-scaled kernel has no
+ * stream-K region.  Past the cluster's last unit, out->tile is -1.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (null pointer, cluster outside
+ * [0, grid / cta_group), negative index) or GEMM_ERR_UNSUPPORTED (a
+ * single-CTA plan, which has no persistent schedule).
+ */
+gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_t* info, int32_t cluster,
+                                  int32_t index, gemm_work_unit_t* out);
+
 /*
  * gemm_run -- enqueue D = A * B^T on `stream` (asynchronous, stream-ordered).
  * A, B, D are device pointers laid out as described at the top of this file;
