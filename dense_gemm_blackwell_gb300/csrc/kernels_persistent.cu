@@ -30,8 +30,9 @@
 // back in two 256-column halves: the MMAs of tile t+1 start on the left half
 // and wait for the right one after kWideLeadStages stages.  The grid is
 // persistent: CTA (pair) c takes tiles c, c+G, ... in a grouped raster that
-// keeps a wave's A and B panels in L2.  Every thread follows the same tile
-// sequence and leaves the loop together.
+// keeps a wave's A and B panels in L2; when the tiles do not fill whole waves,
+// a stream-K region split along K comes first (units.cuh).  Every thread
+// follows the same unit sequence and leaves the loop together.
 //
 // cta_group::2: a cluster of two CTAs on neighbouring SMs computes a
 // (256 x tile_n) tile with one MMA stream issued by the even CTA.  Each CTA
