@@ -35,10 +35,16 @@ METRIC = "GEMM TFLOP/s (bf16 in, fp32 acc, 8192^3) and fraction of GB300 dense p
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 PROFILE = os.path.join(ROOT, "profiles", "persistent_pair_square8192_bf16_f32.md")
+# everything that decides what the headline kernel does: its code, its work
+# schedule and the host code that plans and launches it
 KERNEL_SOURCES = ["dense_gemm_blackwell_gb300/csrc/kernels_persistent.cu",
                   "dense_gemm_blackwell_gb300/csrc/pipeline.cuh",
+                  "dense_gemm_blackwell_gb300/csrc/units.cuh",
                   "dense_gemm_blackwell_gb300/csrc/ptx.cuh",
-                  "dense_gemm_blackwell_gb300/csrc/common.cuh"]
+                  "dense_gemm_blackwell_gb300/csrc/common.cuh",
+                  "dense_gemm_blackwell_gb300/csrc/launch.h",
+                  "dense_gemm_blackwell_gb300/csrc/gemm_api.cu",
+                  "include/gemm.h"]
 
 
 def max_over_ranks(value: float, dist, device) -> float:
