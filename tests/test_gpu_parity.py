@@ -161,6 +161,19 @@ def test_stream_k_integers_bit_exact(cg_flag, M, N, K, ctas, out):
     assert info["stream_k_tiles"] > 0
 
 
+@pytest.mark.parametrize("cg_flag,M,N,K,ctas,out", [
+    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 1000, 1040, 16, "f32"),   # 12 tiles on 8 pairs
+    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 2064, 8, "bf16"),    # 15 tiles on 8 CTAs
+])
+def test_stream_k_only_ragged_bit_exact(cg_flag, M, N, K, ctas, out):
+    """Every tile in the stream-K region, so each finisher is its cluster's
+    last unit and gathers the partial through the operand ring; ragged M, N
+    and K leave some of its chunks (and, past M, whole warps) without work."""
+    prob = inputs.make("square8192_bf16", M=M, N=N, K=K, dist="ints", seed=19)
+    r, info = check_full(prob, out, exact=True, flags=cg_flag, max_ctas=ctas, tile_n=256)
+    assert info["stream_k_tiles"] == info["num_tiles"], info
+
+
 def test_stream_k_matches_data_parallel():
     prob = inputs.make("square4096_bf16", M=1024, N=768, K=2048, seed=18)
     D1, info1 = run_gpu(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
