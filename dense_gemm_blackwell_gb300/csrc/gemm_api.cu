@@ -655,6 +655,11 @@ gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_
     dgb::PersistentParams p{};
     fill_schedule(*desc, *info, p);
     p.sk_tiles = info->kernel == GEMM_KERNEL_PERSISTENT ? info->stream_k_tiles : 0;
+    // info must be this desc's plan: the tile count and the stream-K region
+    // have to agree with the shape, or the raster arithmetic is meaningless
+    if (info->num_tiles != (int64_t)p.tiles_per_batch * std::max<int64_t>(desc->batch, 1) || p.sk_tiles < 0 ||
+        p.sk_tiles > p.num_tiles || (p.sk_tiles > 0 && p.sk_tiles < clusters))
+        return GEMM_ERR_INVALID_ARG;
     gemm_work_unit_t r{};
     r.tile = -1;
     dgb::WorkUnit u;

@@ -208,8 +208,9 @@ typedef struct {
  * asks for next to its table of ridges).  The block-scaled kernel has no
  * stream-K region.  Past the cluster's last unit, out->tile is -1.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (null pointer, cluster outside
- * [0, grid / cta_group), negative index) or GEMM_ERR_UNSUPPORTED (a
- * single-CTA plan, which has no persistent schedule).
+ * [0, grid / cta_group), negative index, or an info whose tile count or
+ * stream-K region does not fit desc) or GEMM_ERR_UNSUPPORTED (a single-CTA
+ * plan, which has no persistent schedule).
  */
 gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_t* info, int32_t cluster,
                                   int32_t index, gemm_work_unit_t* out);

@@ -191,6 +191,14 @@ def test_argument_errors():
     assert dg.gemm_plan_work_unit(desc, info, 0, -1)[0] == dg.GEMM_ERR_INVALID_ARG
     s, u = dg.gemm_plan_work_unit(desc, info, 0, 7)     # cluster 0 has 7 tiles: 0..6
     assert s == dg.GEMM_OK and u.tile == -1
+    # an info that is not this desc's plan
+    other = dg.make_desc(4096, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    assert dg.gemm_plan_work_unit(other, info, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
+    zero_n = dg.make_desc(8192, 0, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    assert dg.gemm_plan_work_unit(zero_n, info, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
+    bad_sk = dg.GemmPlanInfo.from_buffer_copy(info)
+    bad_sk.stream_k_tiles = 5                      # fewer than the 76 clusters
+    assert dg.gemm_plan_work_unit(desc, bad_sk, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
     desc, info = plan(128, 64, 64, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F32)
     assert info.kernel == dg.GEMM_KERNEL_SINGLE_CTA
     assert dg.gemm_plan_work_unit(desc, info, 0, 0)[0] == dg.GEMM_ERR_UNSUPPORTED
