@@ -206,7 +206,9 @@ typedef struct {
  * range from the end), then data-parallel tiles, raster groups of m blocks
  * first (the L2 reuse across a wave that the "Hopper and Blackwell GEMM" page
  * asks for next to its table of ridges).  The block-scaled kernel has no
- * stream-K region.  Past the cluster's last unit, out->tile is -1.
+ * stream-K region (its producers call the same functions; its MMA and
+ * promotion loops step through the same tiles c, c + G, ... directly).
+ * Past the cluster's last unit, out->tile is -1.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (null pointer, cluster outside
  * [0, grid / cta_group), negative index, or an info whose tile count or
  * stream-K region does not fit desc) or GEMM_ERR_UNSUPPORTED (a single-CTA
