@@ -11,7 +11,8 @@ namespace dgb {
 cudaError_t launch_single_cta(const SingleParams& p, int dtype_d, int batch, size_t smem_bytes,
                               cudaStream_t stream);
 
-// Persistent kernel: grid = CTAs (a multiple of cta_group), block = 192 threads.
+// Persistent kernel: grid = CTAs (a multiple of cta_group), block = 352 threads (kThreads: two producer
+// warps, the MMA warp and eight epilogue warps).
 cudaError_t launch_persistent(const PersistentParams& p, int cta_group, int dtype_d, int grid,
                               size_t smem_bytes, cudaStream_t stream);
 
@@ -19,7 +20,8 @@ cudaError_t launch_persistent(const PersistentParams& p, int cta_group, int dtyp
 // memory can be resident at once (0 if the query fails).
 int persistent_max_active_clusters(int cta_group, int dtype_d, size_t smem_bytes);
 
-// Block-scaled e4m3 kernel: grid = CTAs (a multiple of cta_group), block = 320 threads.
+// Block-scaled e4m3 kernel: grid = CTAs (a multiple of cta_group), block = 384 threads (kFp8Threads:
+// producers, MMA warp and an idle warp, then eight promotion/epilogue warps).
 cudaError_t launch_fp8_block(const PersistentParams& p, int cta_group, int dtype_d, int grid, size_t smem_bytes,
                              cudaStream_t stream);
 int fp8_max_active_clusters(int cta_group, int tile_n, int dtype_d, size_t smem_bytes);

@@ -127,3 +127,23 @@ def test_fp8_mn_major_bit_exact(cg_flag, mn_a, mn_b):
     if not r["ok"]:
         dump_on_failure("fp8_mn_%d%d_cg%d" % (mn_a, mn_b, info["cta_group"]), got=got, dref=dref[0], sabs=sabs[0])
     assert r["ok"], (r, info)
+
+
+@pytest.mark.slow
+def test_fp8_full_size_integers_bit_exact():
+    """The benchmark's plan (SM-pair 256 x 256 tiles over the whole grid) on
+    integer codes with scales in {1/2, 1, 2}: each block product, each scaled
+    partial and each running sum is exact in fp32 (below 2^21 in units of
+    1/4), so D must equal the oracle's single rounding bit for bit, on seeded
+    rows plus the first and last row of every 128-row block."""
+    prob = inputs.make("fp8_block8192", dist="ints")
+    D, info = run_fp8(prob, "bf16")
+    assert info["cta_group"] == 2 and info["tile_n"] == 256, info
+    rows = inputs.sample_rows(prob.wl.M, 1, n_random=64, seed=4, tile_m=128)
+    dref, s = oracle_fp8(prob, rows)
+    got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref, s, "bf16", TOL_FP8, exact=True)
+    if not r["ok"]:
+        dump_on_failure("fp8_full_exact", got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+

@@ -254,3 +254,51 @@ def test_full_square4096_bf16_bf16():
 @pytest.mark.slow
 def test_full_batched256_f16():
     check_sampled("batched256_f16", "f16")
+
+
+# ------------------------------------------------------------------ full-size workloads, integer-valued, bit-exact
+#
+# The same shapes, element types and default plans the benchmark times (pair
+# tiles, the whole grid, the raster groups and the serpentine K order), with
+# entries in {-3..3}: every partial sum stays below 9 K <= 73,728 < 2^24 in
+# magnitude, so any fp32 summation order gives the exact sum and the one
+# rounding to D's type must equal the oracle's rounding bit for bit.  A dropped,
+# repeated or misplaced K slice changes some element by an integer and fails.
+
+def check_sampled_exact(name, out_dtype, whole=False, expect=None):
+    prob = inputs.make(name, dist="ints")
+    wl = prob.wl
+    D, info = run_gpu(prob, out_dtype)
+    if expect:
+        assert {k: info[k] for k in expect} == expect, info
+    if whole:
+        dref, s = oracle_rows(prob)
+        got = D.double().cpu().numpy().reshape(dref.shape)
+    else:
+        # seeded random rows plus the first and last row of every 128-row
+        # block (each CTA's own rows, not only the pair tile's edges)
+        rows = inputs.sample_rows(wl.M, wl.batch, n_random=64, seed=3, tile_m=128)
+        dref, s = oracle_rows(prob, rows)
+        got = D.reshape(wl.batch * wl.M, wl.N)[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref, s, out_dtype, TOL_16BIT, exact=True)
+    if not r["ok"]:
+        dump_on_failure("exact_" + name, got=got, dref=dref, sabs=s)
+    assert r["ok"], (name, r, info)
+    return info
+
+
+@pytest.mark.slow
+def test_full_square8192_bf16_f32_integers_bit_exact():
+    check_sampled_exact("square8192_bf16", "f32",
+                        expect={"cta_group": 2, "tile_n": 512, "tmem_stages": 1, "grid": 152, "stream_k_tiles": 0})
+
+
+@pytest.mark.slow
+def test_full_square4096_bf16_bf16_integers_bit_exact():
+    check_sampled_exact("square4096_bf16", "bf16", expect={"cta_group": 2, "tile_n": 512})
+
+
+@pytest.mark.slow
+def test_full_batched256_f16_integers_bit_exact_whole_output():
+    check_sampled_exact("batched256_f16", "f16", whole=True)
+

@@ -4,10 +4,12 @@ they cannot afford the synchronisation an allocation may imply).  Its kernels
 keep their error record in a library-owned static device array instead of a
 plan's cudaMalloc'd record.
 
-Checked through the C ABI against the plan-based gemm_run on the same inputs,
-within the parity tolerance of the other tests, on two calls in a row (the
-second call finds the record left by the first and must clear it).  This file
-is collected last on purpose; it also passes when run alone.
+Checked through the C ABI on two calls in a row (the second call finds the
+record left by the first and must clear it): against the CPU oracle, within
+the parity tolerance of the other tests for random inputs and bit for bit for
+integer-valued inputs, and against the plan-based gemm_run, which must give the
+same bytes (both run the same data-parallel tiles).  This file is collected
+last on purpose; it also passes when run alone.
 """
 import pytest
 import torch
@@ -37,8 +39,11 @@ CODE = {"f32": dg.GEMM_F32, "bf16": dg.GEMM_BF16, "f16": dg.GEMM_F16}
 IN_CODE = {"bf16": dg.GEMM_BF16, "f16": dg.GEMM_F16}
 
 
+@pytest.mark.parametrize("dist", ["random", "ints"])
 @pytest.mark.parametrize("name,over,out,flags", CASES)
-def test_noalloc_matches_gemm_run_on_two_calls(name, over, out, flags):
+def test_noalloc_matches_oracle_on_two_calls(name, over, out, flags, dist):
+    if dist == "ints":
+        over = dict(over, dist="ints")
     prob = inputs.make(name, **over)
     wl = prob.wl
     A, B = prob.A.cuda(), prob.B.cuda()
@@ -46,15 +51,14 @@ def test_noalloc_matches_gemm_run_on_two_calls(name, over, out, flags):
     desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=IN_CODE[wl.dtype_in], dtype_d=CODE[out],
                         flags=flags)
     stream = torch.cuda.current_stream().cuda_stream
-
-    D_ref = torch.empty(shape, dtype=TDT[out], device="cuda")
-    with dg.Plan(desc) as plan:
-        plan.run(A, B, D_ref)
+    dref, sabs = oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, batch=wl.batch,
+                                  dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
+    # the plan-based path on the same data-parallel tiles, for a byte comparison
+    D_plan = torch.empty(shape, dtype=TDT[out], device="cuda")
+    with dg.Plan(dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=IN_CODE[wl.dtype_in],
+                              dtype_d=CODE[out], flags=flags | dg.GEMM_FLAG_NO_STREAM_K)) as plan:
+        plan.run(A, B, D_plan)
         assert plan.sync_status()[0] == dg.GEMM_OK
-
-    _, sabs = oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, batch=wl.batch,
-                               dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
-    ref = D_ref.double().cpu().numpy().reshape(sabs.shape)
     for call in range(2):
         D = torch.full(shape, float("nan"), dtype=TDT[out], device="cuda")
         rec = dg.GemmDeviceError()
@@ -62,9 +66,9 @@ def test_noalloc_matches_gemm_run_on_two_calls(name, over, out, flags):
         assert s == dg.GEMM_OK, (call, dg.gemm_status_string(s))
         assert rec.code == 0
         got = D.double().cpu().numpy().reshape(sabs.shape)
-        # same tolerance as the parity tests, with gemm_run's result as the reference value
-        r = compare(got, ref, sabs, out, TOL_16BIT)
-        assert r["ok"], (call, r)
+        r = compare(got, dref, sabs, out, TOL_16BIT, exact=(dist == "ints"))
+        assert r["ok"], (call, dist, r)
+        assert torch.equal(D, D_plan), call
 
 
 def test_noalloc_enqueue_only_then_sync():
