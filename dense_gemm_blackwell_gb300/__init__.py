@@ -20,6 +20,7 @@ __all__ = [
     "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host", "gemm_run_noalloc",
     "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
     "gemm_version", "gemm_schedule_model", "gemm_schedule_choose", "gemm_plan_work_unit", "GemmWorkUnit", "Plan",
+    "GemmMachine", "gemm_plan_schedule", "gemm_machine_gb300",
     "matmul", "header_functions",
 ]
 
@@ -100,6 +101,12 @@ class GemmSchedResult(ctypes.Structure):
                 ("steady_period", ctypes.c_double), ("stages_needed", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class GemmMachine(ctypes.Structure):
+    _fields_ = [("mma_flops_per_cycle", ctypes.c_double), ("stage_fixed_cycles", ctypes.c_double),
+                ("ingest_bytes_per_cycle", ctypes.c_double), ("load_latency_cycles", ctypes.c_double),
+                ("tmem_read_bytes_per_cycle", ctypes.c_double), ("handback_cycles", ctypes.c_double)]
+
+
 class GemmDeviceError(ctypes.Structure):
     _fields_ = [("code", ctypes.c_uint32), ("role", ctypes.c_uint32), ("stage", ctypes.c_uint32),
                 ("tile", ctypes.c_uint32), ("block", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 3)]
@@ -164,6 +171,13 @@ def lib():
                                                    ctypes.c_double, ctypes.POINTER(ctypes.c_int32),
                                                    ctypes.POINTER(ctypes.c_int32)]
                 L.gemm_schedule_choose.restype = st
+                L.gemm_plan_schedule.argtypes = [ctypes.POINTER(GemmDesc), ctypes.POINTER(GemmPlanInfo),
+                                                 ctypes.POINTER(GemmDeviceProps), ctypes.POINTER(GemmMachine),
+                                                 ctypes.POINTER(GemmSchedParams), ctypes.POINTER(GemmSchedResult),
+                                                 ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+                L.gemm_plan_schedule.restype = st
+                L.gemm_machine_gb300.argtypes = [ctypes.POINTER(GemmMachine)]
+                L.gemm_machine_gb300.restype = st
                 L.gemm_version.restype = st
                 _lib = L
     return _lib
@@ -249,6 +263,25 @@ def gemm_schedule_choose(tiles, k_slices, t_issue, t_load, t_mma, t_epi, max_sta
     st = lib().gemm_schedule_choose(ctypes.byref(p), max_stages, max_accumulators, tolerance,
                                     ctypes.byref(s), ctypes.byref(a))
     return st, s.value, a.value
+
+
+def gemm_plan_schedule(desc: GemmDesc, info: GemmPlanInfo, props: GemmDeviceProps, machine=None):
+    """The schedule model of a planned problem: (status, GemmSchedParams, GemmSchedResult, S, A), S and A
+    being the model's choice within the plan's limits; machine None = the measured GB300 figures."""
+    p, r = GemmSchedParams(), GemmSchedResult()
+    s, a = ctypes.c_int32(), ctypes.c_int32()
+    st = lib().gemm_plan_schedule(ctypes.byref(desc), ctypes.byref(info), ctypes.byref(props),
+                                  ctypes.byref(machine) if machine is not None else None,
+                                  ctypes.byref(p), ctypes.byref(r), ctypes.byref(s), ctypes.byref(a))
+    return st, p, r, s.value, a.value
+
+
+def gemm_machine_gb300() -> GemmMachine:
+    m = GemmMachine()
+    st = lib().gemm_machine_gb300(ctypes.byref(m))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_machine_gb300")
+    return m
 
 
 def gemm_last_cuda_error() -> int:

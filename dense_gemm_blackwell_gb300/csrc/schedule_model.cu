@@ -10,6 +10,7 @@
 // The run ends with the last epilogue; the tensor core is busy T*K*t_mma of it.
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <vector>
 
 #include "gemm.h"
@@ -92,6 +93,81 @@ gemm_status_t gemm_schedule_choose(const gemm_sched_params_t* in, int32_t max_st
     }
     *stages = max_stages;
     *accumulators = max_accumulators;
+    return GEMM_OK;
+}
+
+// Unit costs measured on GB300 (SM clock cycles):
+//  * 8,192 flop per cycle per SM for kind::f16 (a probe issuing M128 N256 K16
+//    MMAs back to back: 128 cycles each);
+//  * copy path 400 cycles per ring stage plus 128 bytes per cycle: a scratch
+//    copy of the persistent kernel with its MMAs skipped streamed 8192^3's
+//    operands at 657 cycles per 32 KB stage and 912 per 64 KB stage;
+//  * tcgen05.ld 220 bytes per cycle per SM while the MMAs run (200-240 measured);
+//  * load latency 900 and hand-back 600 cycles: estimates (the model's runs at
+//    three or more stages and two accumulators do not depend on them).
+constexpr gemm_machine_t kGb300 = {8192.0, 400.0, 128.0, 900.0, 220.0, 600.0};
+
+gemm_status_t gemm_machine_gb300(gemm_machine_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = kGb300;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_schedule(const gemm_desc_t* desc, const gemm_plan_info_t* info,
+                                 const gemm_device_props_t* props, const gemm_machine_t* machine,
+                                 gemm_sched_params_t* params, gemm_sched_result_t* result,
+                                 int32_t* model_stages, int32_t* model_accumulators) {
+    if (!desc || !info || !props) return GEMM_ERR_INVALID_ARG;
+    if (info->kernel != GEMM_KERNEL_PERSISTENT) return GEMM_ERR_UNSUPPORTED;
+    const gemm_machine_t& mc = machine ? *machine : kGb300;
+    if (!(mc.mma_flops_per_cycle > 0) || !(mc.ingest_bytes_per_cycle > 0) || !(mc.tmem_read_bytes_per_cycle > 0) ||
+        mc.stage_fixed_cycles < 0 || mc.load_latency_cycles < 0 || mc.handback_cycles < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (info->cta_group < 1 || info->grid < info->cta_group || info->tile_n <= 0 || info->tile_k <= 0 ||
+        info->stages < 1 || info->tmem_stages < 1 || info->num_tiles < 1 || info->stage_bytes <= 0 || desc->K <= 0)
+        return GEMM_ERR_INVALID_ARG;
+    const int64_t clusters = info->grid / info->cta_group;
+    const int64_t k_slices = (desc->K + info->tile_k - 1) / info->tile_k;
+    int64_t tiles = (info->num_tiles + clusters - 1) / clusters;
+    if (info->stream_k_tiles > 0) {
+        // a cluster's share of all K slices, counted in whole tiles
+        const int64_t slices = (info->num_tiles * k_slices + clusters - 1) / clusters;
+        tiles = (slices + k_slices - 1) / k_slices;
+    }
+    if (tiles > (1 << 20) || k_slices > (1 << 20) || tiles * k_slices > (1 << 24)) return GEMM_ERR_UNSUPPORTED;
+    // tf32 multiplies at half the 16-bit rate (nominal 1.1 against 2.25 PFLOP/s)
+    const double rate = mc.mma_flops_per_cycle * (desc->dtype_a == GEMM_TF32 ? 0.5 : 1.0);
+    gemm_sched_params_t p{};
+    p.tiles = (int32_t)tiles;
+    p.k_slices = (int32_t)k_slices;
+    p.stages = info->stages;
+    p.accumulators = info->tmem_stages;
+    const double stage_bytes = (double)info->stage_bytes;   // per CTA, A and B
+    p.t_mma = 2.0 * 128.0 * info->tile_n * info->tile_k / rate;
+    p.t_issue = mc.stage_fixed_cycles + stage_bytes / mc.ingest_bytes_per_cycle;
+    p.t_load = mc.load_latency_cycles + stage_bytes / mc.ingest_bytes_per_cycle;
+    p.t_epi = 128.0 * info->tile_n * 4.0 / mc.tmem_read_bytes_per_cycle + mc.handback_cycles;
+    if (params) *params = p;
+    if (result) {
+        gemm_status_t st = gemm_schedule_model(&p, result);
+        if (st != GEMM_OK) return st;
+    }
+    if (model_stages || model_accumulators) {
+        // the planner's limits: as many stages as the shared memory holds
+        // (each costs its bytes and two 8-byte barriers), two accumulators up
+        // to 256 columns and one for 512-wide tiles
+        int64_t max_s = info->stages;
+        if (props->smem_optin_bytes > 0)
+            while (max_s < 16 && info->smem_bytes + (max_s + 1 - info->stages) * (info->stage_bytes + 16) <=
+                                     props->smem_optin_bytes)
+                ++max_s;
+        const int32_t max_a = info->tile_n > 256 ? 1 : 2;
+        int32_t s = 0, a = 0;
+        gemm_status_t st = gemm_schedule_choose(&p, (int32_t)max_s, max_a, 0.005, &s, &a);
+        if (st != GEMM_OK) return st;
+        if (model_stages) *model_stages = s;
+        if (model_accumulators) *model_accumulators = a;
+    }
     return GEMM_OK;
 }
 

@@ -344,6 +344,49 @@ gemm_status_t gemm_schedule_model(const gemm_sched_params_t* in, gemm_sched_resu
 gemm_status_t gemm_schedule_choose(const gemm_sched_params_t* in, int32_t max_stages, int32_t max_accumulators,
                                    double tolerance, int32_t* stages, int32_t* accumulators);
 
+/* Unit costs of one SM, in SM clock cycles, from which gemm_plan_schedule
+ * derives the schedule model's times for a plan. */
+typedef struct {
+    double mma_flops_per_cycle;       /* tensor core, kind::f16 (bf16/f16 inputs); tf32 runs at half, 8-bit
+                                         inputs at twice this rate */
+    double stage_fixed_cycles;        /* copy path: cost of one ring stage beyond its bytes */
+    double ingest_bytes_per_cycle;    /* copy path: operand bytes per cycle into one SM's shared memory */
+    double load_latency_cycles;       /* from a stage's copies being issued to its first bytes landing */
+    double tmem_read_bytes_per_cycle; /* epilogue: tcgen05.ld bytes per cycle per SM */
+    double handback_cycles;           /* epilogue: fixed cost of handing an accumulator back to the MMA warp */
+} gemm_machine_t;
+
+/*
+ * gemm_plan_schedule -- the schedule model ("Hopper and Blackwell GEMM",
+ * section "Maths"; see gemm_schedule_model) applied to a planned persistent
+ * 16-bit/tf32 problem.  From the plan's tile, stage depth and accumulator count
+ * and a machine's unit costs (NULL: the GB300 figures this library measured,
+ * see gemm_machine_gb300) it derives, per SM (pair):
+ *   tiles      T = ceil(output tiles / clusters) (stream-K plans: the K slices of
+ *                  one cluster's share, in whole tiles)
+ *   k_slices   K = ceil(K / tile_k)
+ *   t_mma      = 2 * 128 * tile_n * tile_k / mma rate
+ *   t_issue    = stage_fixed + stage_bytes / ingest      (the copy path's throughput)
+ *   t_load     = load_latency + stage_bytes / ingest     (one stage's data in)
+ *   t_epi      = 128 * tile_n * 4 / tmem_read + handback (an accumulator's read-back)
+ * fills *params (may be NULL) and evaluates the model into *result (may be
+ * NULL), in cycles.  *model_stages / *model_accumulators (may be NULL) receive
+ * gemm_schedule_choose's pick, tolerance 0.5 %, within the plan's limits:
+ * the ring depth the shared memory of `props` holds and the accumulators its
+ * tensor memory and kernel support (two up to 256 columns, one for 512-wide
+ * tiles).  Host arithmetic only.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, or GEMM_ERR_UNSUPPORTED for plans
+ * other than GEMM_KERNEL_PERSISTENT.
+ */
+gemm_status_t gemm_plan_schedule(const gemm_desc_t* desc, const gemm_plan_info_t* info,
+                                 const gemm_device_props_t* props, const gemm_machine_t* machine,
+                                 gemm_sched_params_t* params, gemm_sched_result_t* result,
+                                 int32_t* model_stages, int32_t* model_accumulators);
+
+/* gemm_machine_gb300 -- the unit costs measured on GB300 with this library's
+ * kernels and probes (clock64 and CUDA events; values in cycles at the SM clock). */
+gemm_status_t gemm_machine_gb300(gemm_machine_t* out);
+
 /* gemm_plan_destroy -- free the plan and its status record (NULL is allowed). */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
