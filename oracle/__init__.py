@@ -27,11 +27,13 @@ _lock = threading.Lock()
 _lib = None
 
 # element type codes of oracle.c
-F16, BF16, E4M3, F32, E5M2 = 0, 1, 2, 3, 4
+F16, BF16, E4M3, F32, E5M2, E2M1, E8M0 = 0, 1, 2, 3, 4, 5, 6
 _NAMES = {"f16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16,
           "e4m3": E4M3, "float8_e4m3fn": E4M3, "f32": F32, "float32": F32,
-          "e5m2": E5M2, "float8_e5m2": E5M2}
-_BYTES = {F16: 2, BF16: 2, E4M3: 1, F32: 4, E5M2: 1}
+          "e5m2": E5M2, "float8_e5m2": E5M2, "e2m1": E2M1, "e8m0": E8M0}
+_BYTES = {F16: 2, BF16: 2, E4M3: 1, F32: 4, E5M2: 1, E2M1: 1, E8M0: 1}
+# scale kinds of oracle.c (orc_problem.scaled)
+_SCALE_KINDS = {None: 0, "fp32_block": 1, "mx": 2, "nv": 3}
 
 
 def dtype_code(name) -> int:
@@ -50,6 +52,7 @@ class _Problem(ctypes.Structure):
         ("scaled", ctypes.c_int32), ("pad_", ctypes.c_int32),
         ("ld_sa", ctypes.c_int64), ("ld_sb", ctypes.c_int64),
         ("stride_sa", ctypes.c_int64), ("stride_sb", ctypes.c_int64),
+        ("tensor_scale_a", ctypes.c_double), ("tensor_scale_b", ctypes.c_double),
     ]
 
 
@@ -137,13 +140,18 @@ def _raw(x, dtype):
 def gemm_rows(A, B, *, M, N, K, dtype_a, dtype_b, batch=1, major_a="k", major_b="k",
               lda=None, ldb=None, stride_a=None, stride_b=None,
               scale_a=None, scale_b=None, ld_sa=None, ld_sb=None, stride_sa=0, stride_sb=0,
-              rows=None):
+              scale_mode=None, tensor_scales=(1.0, 1.0), rows=None):
     """Reference rows of D and of S = sum |a*b|.
 
     ``A``/``B`` hold raw element codes (numpy arrays or torch CPU tensors) laid
-    out as described in ``oracle.c``.  ``rows`` is a list of flat row indices
-    ``b*M + m`` (``None`` = all rows).  Returns ``(D_ref, S)`` as float64 arrays
-    of shape ``(len(rows), N)`` (or ``(batch, M, N)`` when ``rows`` is None).
+    out as described in ``oracle.c``; 4-bit E2M1 operands are bytes holding
+    two elements each (``lda``/``ldb``/strides still count elements).
+    ``scale_mode``: None (no scales, or fp32 block scales when ``scale_a`` is
+    given), "mx" (E8M0 per 32) or "nv" (E4M3 per 16 times ``tensor_scales``);
+    MX/NV scales are the tiled scale bytes, ``stride_sa``/``stride_sb`` the
+    bytes between batch entries (0 = packed).  ``rows`` is a list of flat row
+    indices ``b*M + m`` (``None`` = all rows).  Returns ``(D_ref, S)`` as
+    float64 arrays of shape ``(len(rows), N)`` (or ``(batch, M, N)``).
     """
     lib = _load()
     ka = major_a in ("k", 0)
@@ -160,7 +168,13 @@ def gemm_rows(A, B, *, M, N, K, dtype_a, dtype_b, batch=1, major_a="k", major_b=
     b = _raw(B, dtype_b)
     sa = sb = None
     p.scaled = 0
-    if scale_a is not None or scale_b is not None:
+    p.tensor_scale_a, p.tensor_scale_b = float(tensor_scales[0]), float(tensor_scales[1])
+    if scale_mode in ("mx", "nv"):
+        p.scaled = _SCALE_KINDS[scale_mode]
+        sa = _raw(scale_a, "e8m0")
+        sb = _raw(scale_b, "e8m0")
+        p.stride_sa, p.stride_sb = stride_sa, stride_sb
+    elif scale_a is not None or scale_b is not None:
         p.scaled = 1
         sa = np.ascontiguousarray(np.asarray(scale_a, dtype=np.float32)).reshape(-1)
         sb = np.ascontiguousarray(np.asarray(scale_b, dtype=np.float32)).reshape(-1)
