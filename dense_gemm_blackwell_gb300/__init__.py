@@ -17,7 +17,8 @@ from ._build import LIB as _LIB_PATH, build as _build
 
 __all__ = [
     "build", "lib", "GemmError", "GemmDesc", "GemmPlanInfo", "GemmDeviceProps", "GemmDeviceError",
-    "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_host", "gemm_run_noalloc",
+    "gemm_plan_query", "gemm_plan_create", "gemm_plan_info", "gemm_run", "gemm_run_mx", "gemm_run_host",
+    "gemm_run_noalloc",
     "gemm_sync_status", "gemm_plan_destroy", "gemm_status_string", "gemm_last_cuda_error",
     "gemm_version", "gemm_schedule_model", "gemm_schedule_choose", "gemm_plan_work_unit", "GemmWorkUnit", "Plan",
     "GemmMachine", "gemm_plan_schedule", "gemm_machine_gb300",
@@ -27,10 +28,11 @@ __all__ = [
 # ---------------------------------------------------------------- constants (include/gemm.h)
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE, GEMM_ERR_RESOURCES = 4, 5, 6, 7
-GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32, GEMM_E5M2, GEMM_TF32 = 0, 1, 2, 3, 4, 5
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32, GEMM_E5M2, GEMM_TF32, GEMM_E2M1 = 0, 1, 2, 3, 4, 5, 6
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
-GEMM_SCALE_NONE, GEMM_SCALE_BLOCK_1x128_128x128 = 0, 1
+GEMM_SCALE_NONE, GEMM_SCALE_BLOCK_1x128_128x128, GEMM_SCALE_MX_E8M0_32, GEMM_SCALE_NV_E4M3_16 = 0, 1, 2, 3
 GEMM_KERNEL_SINGLE_CTA, GEMM_KERNEL_PERSISTENT, GEMM_KERNEL_FP8_BLOCK, GEMM_KERNEL_ZERO_FILL = 1, 2, 3, 4
+GEMM_KERNEL_MX = 5
 GEMM_FLAG_CTA_GROUP_1 = 1 << 0
 GEMM_FLAG_CTA_GROUP_2 = 1 << 1
 GEMM_FLAG_NO_SINGLE_CTA = 1 << 2
@@ -153,6 +155,8 @@ def lib():
                 L.gemm_plan_work_unit.restype = st
                 L.gemm_run.argtypes = [vp, vp, vp, vp, vp, vp, vp]
                 L.gemm_run.restype = st
+                L.gemm_run_mx.argtypes = [vp] * 8
+                L.gemm_run_mx.restype = st
                 L.gemm_run_host.argtypes = [vp] * 12
                 L.gemm_run_host.restype = st
                 L.gemm_run_noalloc.argtypes = [ctypes.POINTER(GemmDesc), vp, vp, vp, vp, vp, vp,
@@ -222,6 +226,11 @@ def gemm_plan_work_unit(desc: GemmDesc, info: GemmPlanInfo, cluster: int, index:
 
 def gemm_run(plan, A, B, D, scale_a=None, scale_b=None, stream=None) -> int:
     return lib().gemm_run(plan, A, B, D, scale_a, scale_b, stream)
+
+
+def gemm_run_mx(plan, A, B, D, sf_a, sf_b, tensor_scales=None, stream=None) -> int:
+    """Hardware block-scaled product (MX / NVFP4 plans); pointers are device addresses."""
+    return lib().gemm_run_mx(plan, A, B, D, sf_a, sf_b, tensor_scales, stream)
 
 
 def gemm_run_host(plan, hA, hB, hD, hsa, hsb, dA, dB, dD, dsa, dsb, stream=None) -> int:
@@ -357,6 +366,16 @@ class Plan:
                            None if scale_b is None else scale_b.data_ptr(), stream)
         if s != GEMM_OK:
             raise GemmError(s, "gemm_run")
+
+    def run_mx(self, A, B, D, sf_a, sf_b, tensor_scales=None, stream=None):
+        """Enqueue an MX / NVFP4 product: sf_a, sf_b are the tiled scale bytes and
+        tensor_scales (NVFP4 only) a 2-element fp32 tensor, all torch CUDA tensors."""
+        if stream is None:
+            stream = current_stream_handle()
+        s = lib().gemm_run_mx(self.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), sf_a.data_ptr(),
+                              sf_b.data_ptr(), None if tensor_scales is None else tensor_scales.data_ptr(), stream)
+        if s != GEMM_OK:
+            raise GemmError(s, "gemm_run_mx")
 
     def run_host(self, hA, hB, hD, dA, dB, dD, hsa=None, hsb=None, dsa=None, dsb=None, stream=None):
         if stream is None:

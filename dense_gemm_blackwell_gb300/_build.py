@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdgb_gemm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["kernels_single.cu", "kernels_persistent.cu", "kernels_fp8.cu", "gemm_api.cu", "schedule_model.cu"]
+SOURCES = ["kernels_single.cu", "kernels_persistent.cu", "kernels_fp8.cu", "kernels_mx.cu", "gemm_api.cu",
+           "schedule_model.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC]

@@ -28,6 +28,7 @@
 #include "gemm.h"
 #include "common.cuh"
 #include "launch.h"
+#include "mx_ptx.cuh"
 #include "units.cuh"
 
 namespace {
@@ -67,6 +68,10 @@ int elem_bytes(int dt) {
 }
 
 bool is8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
+bool is4(int dt) { return dt == GEMM_E2M1; }
+// Scale modes whose scales the tensor core applies (tiled scale bytes, gemm_run_mx).
+bool hw_scaled(int mode) { return mode == GEMM_SCALE_MX_E8M0_32 || mode == GEMM_SCALE_NV_E4M3_16; }
+bool known_dtype(int dt) { return elem_bytes(dt) != 0 || is4(dt); }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -86,13 +91,16 @@ gemm_status_t resolve(const gemm_desc_t* in, Resolved* out) {
     if (!in || !out) return GEMM_ERR_INVALID_ARG;
     gemm_desc_t d = *in;
     if (d.M < 0 || d.N < 0 || d.K < 0 || d.batch < 0) return GEMM_ERR_INVALID_ARG;
-    if (elem_bytes(d.dtype_a) == 0 || elem_bytes(d.dtype_b) == 0 || elem_bytes(d.dtype_d) == 0)
+    if (!known_dtype(d.dtype_a) || !known_dtype(d.dtype_b) || elem_bytes(d.dtype_d) == 0)
         return GEMM_ERR_INVALID_ARG;
     if ((d.major_a != GEMM_K_MAJOR && d.major_a != GEMM_MN_MAJOR) ||
         (d.major_b != GEMM_K_MAJOR && d.major_b != GEMM_MN_MAJOR))
         return GEMM_ERR_INVALID_ARG;
-    if (d.scale_mode != GEMM_SCALE_NONE && d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128)
+    if (d.scale_mode != GEMM_SCALE_NONE && d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128 &&
+        !hw_scaled(d.scale_mode))
         return GEMM_ERR_INVALID_ARG;
+    // tiled scales have a fixed layout: no leading dims
+    if (hw_scaled(d.scale_mode) && (d.ld_sa != 0 || d.ld_sb != 0)) return GEMM_ERR_INVALID_ARG;
     if (d.M > INT32_MAX || d.N > INT32_MAX || d.K > INT32_MAX || d.batch > INT32_MAX)
         return GEMM_ERR_UNSUPPORTED;
     const bool ka = d.major_a == GEMM_K_MAJOR, kb = d.major_b == GEMM_K_MAJOR;
@@ -107,11 +115,19 @@ gemm_status_t resolve(const gemm_desc_t* in, Resolved* out) {
     if (d.stride_d == 0) d.stride_d = d.M * d.ldd;
     if (d.stride_a < 0 || d.stride_b < 0 || d.stride_d < 0) return GEMM_ERR_INVALID_ARG;
     if (d.batch > 1 && d.stride_d < d.M * d.ldd) return GEMM_ERR_INVALID_ARG;  // outputs would overlap
-    const int64_t kblk = std::max<int64_t>(ceil_div(d.K, 128), 1);
-    if (d.ld_sa == 0) d.ld_sa = kblk;
-    if (d.ld_sb == 0) d.ld_sb = kblk;
-    if (d.stride_sa == 0) d.stride_sa = d.M * d.ld_sa;
-    if (d.stride_sb == 0) d.stride_sb = ceil_div(d.N, 128) * d.ld_sb;
+    if (hw_scaled(d.scale_mode)) {
+        // bytes of one batch entry's scale tiles: 512 per 128 rows x 4 scale columns
+        const int64_t v = d.scale_mode == GEMM_SCALE_MX_E8M0_32 ? 32 : 16;
+        const int64_t kq = std::max<int64_t>(ceil_div(ceil_div(d.K, v), 4), 1);
+        if (d.stride_sa == 0) d.stride_sa = std::max<int64_t>(ceil_div(d.M, 128), 1) * kq * 512;
+        if (d.stride_sb == 0) d.stride_sb = std::max<int64_t>(ceil_div(d.N, 128), 1) * kq * 512;
+    } else {
+        const int64_t kblk = std::max<int64_t>(ceil_div(d.K, 128), 1);
+        if (d.ld_sa == 0) d.ld_sa = kblk;
+        if (d.ld_sb == 0) d.ld_sb = kblk;
+        if (d.stride_sa == 0) d.stride_sa = d.M * d.ld_sa;
+        if (d.stride_sb == 0) d.stride_sb = ceil_div(d.N, 128) * d.ld_sb;
+    }
     if (d.wait_timeout_ns == 0) d.wait_timeout_ns = kDefaultTimeoutNs;
     if (d.tile_n < 0 || d.stages < 0 || d.max_ctas < 0) return GEMM_ERR_INVALID_ARG;
     if ((d.flags & GEMM_FLAG_CTA_GROUP_1) && (d.flags & GEMM_FLAG_CTA_GROUP_2)) return GEMM_ERR_INVALID_ARG;
@@ -228,12 +244,90 @@ gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, g
     return GEMM_OK;
 }
 
+// Hardware block-scaled kernel (MXFP8, MXFP4, NVFP4): 256-column tiles, one
+// 128-byte K atom per ring stage (128 8-bit or 256 4-bit elements), scale
+// slabs per stage (A's 128 rows, B's two 128-row blocks), one 256-column
+// accumulator plus a scale slot per stage in tensor memory, 8 epilogue warps
+// with one 4 KB staging buffer each.
+constexpr int kMxThreads = 384;
+constexpr int kMxTileN = 256;
+constexpr int kMxSfColumns = 256;                  // tensor-memory columns left for the scale slots
+
+// 1 = mxf8f6f4, 2 = mxf4, 3 = mxf4nvf4 (the kernel's KIND)
+int mx_kind(const gemm_desc_t& d) {
+    if (d.scale_mode == GEMM_SCALE_NV_E4M3_16) return 3;
+    return is4(d.dtype_a) ? 2 : 1;
+}
+
+// 512-byte scale slabs per 128 rows per ring stage: MXFP8 4 scales of 32
+// (128 elements), MXFP4 8 of 32 (256 elements), NVFP4 16 of 16.
+int mx_chunks(const gemm_desc_t& d) {
+    const int kind = mx_kind(d);
+    return kind == 1 ? 1 : (kind == 2 ? 2 : 4);
+}
+
+gemm_status_t plan_mx(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
+    if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
+    if (d.tile_n != 0 && d.tile_n != kMxTileN) return GEMM_ERR_UNSUPPORTED;
+    if (d.flags & (GEMM_FLAG_SINGLE_CTA | GEMM_FLAG_ACCUM_F16 | GEMM_FLAG_STAGE_K2 | GEMM_FLAG_EPILOGUE_DIRECT))
+        return GEMM_ERR_UNSUPPORTED;
+    const bool fp4 = is4(d.dtype_a);
+    if (fp4 && (d.K % 2 != 0)) return GEMM_ERR_UNSUPPORTED;     // whole bytes of packed elements
+    int cg;
+    if (d.flags & GEMM_FLAG_CTA_GROUP_1) cg = 1;
+    else if (d.flags & GEMM_FLAG_CTA_GROUP_2) cg = 2;
+    else cg = (d.M > 128 && ceil_div(d.M, 256) * ceil_div(d.N, kMxTileN) * d.batch >= props.sm_count / 2) ? 2 : 1;
+    const int chunks = mx_chunks(d);
+    const int64_t stage_a = 128 * 128, stage_b = (kMxTileN / cg) * 128;
+    const int64_t sf_stage = 3 * chunks * 512;
+    // the staging buffers after the scale ring start on a 1024-byte boundary (128-byte swizzle)
+    auto smem_for = [&](int64_t s) {
+        return round_up(s * (stage_a + stage_b + sf_stage), 1024) + kStagingBytes + 8 * (2 * s + 3) + 8 + kAlignSlack;
+    };
+    // tensor memory: 12 columns per slab and stage (A 4, B 8) after the accumulator
+    const int64_t max_by_tmem = kMxSfColumns / (12 * chunks);
+    int64_t stages = d.stages;
+    if (stages == 0) {
+        stages = std::min<int64_t>(16, max_by_tmem);
+        while (stages > 2 && smem_for(stages) > props.smem_optin_bytes) --stages;
+    }
+    if (stages < 2 || stages > 16 || stages > max_by_tmem) return GEMM_ERR_UNSUPPORTED;
+    if (smem_for(stages) > props.smem_optin_bytes) return GEMM_ERR_RESOURCES;
+    const int64_t tiles = ceil_div(d.M, 128 * cg) * ceil_div(d.N, kMxTileN) * d.batch;
+    if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    int64_t clusters = props.sm_count / cg;
+    if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
+    clusters = std::min<int64_t>(clusters, tiles);
+    info->kernel = GEMM_KERNEL_MX;
+    info->cta_group = cg;
+    info->tile_m = 128 * cg;
+    info->tile_n = kMxTileN;
+    info->tile_k = fp4 ? 256 : 128;                   // elements of K per ring stage (one 128-byte atom)
+    info->stages = (int32_t)stages;
+    info->tmem_stages = 1;
+    info->tmem_cols = 512;
+    info->grid = (int32_t)(clusters * cg);
+    info->block_threads = kMxThreads;
+    info->num_tiles = tiles;
+    info->stage_bytes = stage_a + stage_b + sf_stage;
+    info->pipeline_bytes = stages * info->stage_bytes + 8 * (2 * stages + 2) + 4;
+    info->smem_bytes = smem_for(stages);
+    return GEMM_OK;
+}
+
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info);
 
 gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
     std::memset(info, 0, sizeof(*info));
     if (d.dtype_d != GEMM_F32 && d.dtype_d != GEMM_BF16 && d.dtype_d != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
-    if (is8(d.dtype_a) && is8(d.dtype_b)) {
+    const bool hw = hw_scaled(d.scale_mode);
+    if (hw) {
+        // MX: E4M3/E5M2 in any pairing, or E2M1 with E2M1; NV: E2M1 with E2M1
+        const bool f8 = is8(d.dtype_a) && is8(d.dtype_b), f4 = is4(d.dtype_a) && is4(d.dtype_b);
+        if (!(f4 || (f8 && d.scale_mode == GEMM_SCALE_MX_E8M0_32))) return GEMM_ERR_UNSUPPORTED;
+    } else if (is4(d.dtype_a) || is4(d.dtype_b)) {
+        return GEMM_ERR_UNSUPPORTED;     // E2M1 only with hardware block scales
+    } else if (is8(d.dtype_a) && is8(d.dtype_b)) {
         // e4m3 / e5m2 in any pairing, block-scaled only
         if (d.scale_mode != GEMM_SCALE_BLOCK_1x128_128x128) return GEMM_ERR_UNSUPPORTED;
     } else if (d.dtype_a != d.dtype_b) {
@@ -250,6 +344,8 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
         info->cta_group = 1;
         return GEMM_OK;
     }
+
+    if (hw) return plan_mx(d, props, info);
 
     // fp16 accumulation: f16 inputs, persistent kernel, data-parallel tiles
     const bool acc16 = (d.flags & GEMM_FLAG_ACCUM_F16) != 0;
@@ -420,6 +516,27 @@ bool encode_map(CUtensorMap* m, int dt, const void* base, int64_t cols, int64_t 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Scale tiles of a matrix with `rows` rows as a 4-D map of 32-bit words: 128
+// words (one 512-byte slab of 128 rows x 4 scales), kq slabs along K,
+// ceil(rows/128) row blocks, batch entries `batch_stride` bytes apart.  Box
+// (128, chunks, 1, 1): one ring stage's slabs of one row block.  Slabs past
+// the end along K or past the last row block read as zeros.
+bool encode_sf_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kq, int64_t batch, int64_t batch_stride,
+                   int chunks) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const int64_t rb = ceil_div(rows, 128);
+    cuuint64_t dims[4] = {128, (cuuint64_t)kq, (cuuint64_t)rb, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {512, (cuuint64_t)(kq * 512),
+                             (cuuint64_t)std::max<int64_t>(batch_stride, rb * kq * 512)};
+    cuuint32_t box[4] = {128, (cuuint32_t)chunks, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Stream-K for the 16-bit persistent kernel: when the tiles do not fill whole
 // waves of clusters, the last wave plus one full wave (sk_tiles >= clusters)
 // are split evenly along K over all clusters; the rest stays data-parallel.
@@ -467,6 +584,8 @@ gemm_status_t cap_resident(const gemm_desc_t& d, gemm_plan_info_t* info) {
         resident = dgb::persistent_max_active_clusters(info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
     else if (info->kernel == GEMM_KERNEL_FP8_BLOCK)
         resident = dgb::fp8_max_active_clusters(info->cta_group, info->tile_n, d.dtype_d, (size_t)info->smem_bytes);
+    else if (info->kernel == GEMM_KERNEL_MX)
+        resident = dgb::mx_max_active_clusters(mx_kind(d), info->cta_group, d.dtype_d, (size_t)info->smem_bytes);
     else
         return GEMM_OK;
     if (resident <= 0) return cuda_fail(cudaGetLastError());
@@ -552,6 +671,9 @@ struct gemm_plan_s {
     uint32_t* sk_flags;
     float* sk_partials;
     HostPipe* pipe = nullptr;     // gemm_run_host's panels (owned; sub-plans share `status`)
+    CUtensorMap sf_maps[2];       // MX / NV: scale-tile maps of A and B for sf_ptrs
+    const void* sf_ptrs[2] = {nullptr, nullptr};
+    bool sf_valid = false;
 };
 
 static void host_pipe_free(HostPipe* hp) {
@@ -646,7 +768,9 @@ gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info) {
 gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_t* info, int32_t cluster,
                                   int32_t index, gemm_work_unit_t* out) {
     if (!desc || !info || !out || index < 0) return GEMM_ERR_INVALID_ARG;
-    if (info->kernel != GEMM_KERNEL_PERSISTENT && info->kernel != GEMM_KERNEL_FP8_BLOCK) return GEMM_ERR_UNSUPPORTED;
+    if (info->kernel != GEMM_KERNEL_PERSISTENT && info->kernel != GEMM_KERNEL_FP8_BLOCK &&
+        info->kernel != GEMM_KERNEL_MX)
+        return GEMM_ERR_UNSUPPORTED;
     if (info->cta_group < 1 || info->grid < info->cta_group || info->tile_m <= 0 || info->tile_n <= 0 ||
         info->tile_k <= 0 || desc->M < 0 || desc->N < 0 || desc->K < 0)
         return GEMM_ERR_INVALID_ARG;
@@ -685,6 +809,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const gemm_desc_t& d = plan->desc;
     const gemm_plan_info_t& info = plan->info;
+    if (hw_scaled(d.scale_mode)) return GEMM_ERR_INVALID_ARG;     // gemm_run_mx runs these plans
     if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
     if (!D) return GEMM_ERR_INVALID_ARG;
     if (!aligned16(D)) return GEMM_ERR_ALIGNMENT;
@@ -809,6 +934,107 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D, 
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
 }
 
+gemm_status_t gemm_run_mx(gemm_plan_t plan, const void* A, const void* B, void* D, const void* sf_a,
+                          const void* sf_b, const float* tensor_scales, gemm_stream_t stream_) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const gemm_desc_t& d = plan->desc;
+    const gemm_plan_info_t& info = plan->info;
+    if (!hw_scaled(d.scale_mode)) return GEMM_ERR_INVALID_ARG;     // gemm_run runs the other plans
+    const bool nv = d.scale_mode == GEMM_SCALE_NV_E4M3_16;
+    if (nv != (tensor_scales != nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
+    if (!D) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(D)) return GEMM_ERR_ALIGNMENT;
+    const int eb_d = elem_bytes(d.dtype_d);
+    if (((d.ldd * eb_d) & 15) || ((d.batch > 1) && ((d.stride_d * eb_d) & 15))) return GEMM_ERR_ALIGNMENT;
+    cudaError_t e;
+    if (info.kernel == GEMM_KERNEL_ZERO_FILL) {
+        e = dgb::launch_zero_fill(D, d.dtype_d, d.M, d.N, d.batch, d.ldd, d.stride_d, plan->props.sm_count, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+    if (info.kernel != GEMM_KERNEL_MX) return GEMM_ERR_INVALID_ARG;
+    if (!A || !B || !sf_a || !sf_b) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(sf_a) || !aligned16(sf_b)) return GEMM_ERR_ALIGNMENT;
+    if (nv && (reinterpret_cast<uintptr_t>(tensor_scales) & 3u)) return GEMM_ERR_ALIGNMENT;
+    // operands as byte matrices: K bytes per row (E2M1: two elements per byte)
+    const bool fp4 = is4(d.dtype_a);
+    if (fp4 && ((d.lda | d.ldb | d.stride_a | d.stride_b) & 1)) return GEMM_ERR_INVALID_ARG;
+    const int64_t kbytes = fp4 ? d.K / 2 : d.K;
+    const int64_t lda_b = fp4 ? d.lda / 2 : d.lda, ldb_b = fp4 ? d.ldb / 2 : d.ldb;
+    const int64_t sta_b = fp4 ? d.stride_a / 2 : d.stride_a, stb_b = fp4 ? d.stride_b / 2 : d.stride_b;
+    if ((lda_b & 15) || (ldb_b & 15)) return GEMM_ERR_ALIGNMENT;
+    if (d.batch > 1 && ((sta_b & 15) || (stb_b & 15) || (d.stride_sa & 15) || (d.stride_sb & 15)))
+        return GEMM_ERR_ALIGNMENT;
+    const int cg = info.cta_group;
+    const int chunks = mx_chunks(d);
+    const int64_t v = nv ? 16 : 32;
+    const int64_t kq = std::max<int64_t>(ceil_div(ceil_div(d.K, v), 4), 1);
+    if (!plan->maps_valid || plan->map_ptrs[0] != A || plan->map_ptrs[1] != B || plan->map_ptrs[2] != D) {
+        plan->maps_valid = false;
+        // byte boxes of one 128-byte K atom x 128 rows (A) or 256 / cg rows (B)
+        if (!encode_map(&plan->maps[0], GEMM_E4M3, A, kbytes, d.M, lda_b, d.batch, sta_b, 128, 128) ||
+            !encode_map(&plan->maps[1], GEMM_E4M3, B, kbytes, d.N, ldb_b, d.batch, stb_b, 128, kMxTileN / cg) ||
+            !encode_map(&plan->maps[2], d.dtype_d, D, d.N, d.M, d.ldd, d.batch, d.stride_d, 128 / eb_d, 32)) {
+            g_last_cuda_error = (int)cudaErrorInvalidValue;
+            return GEMM_ERR_CUDA;
+        }
+        plan->map_ptrs[0] = A;
+        plan->map_ptrs[1] = B;
+        plan->map_ptrs[2] = D;
+        plan->maps_valid = true;
+    }
+    if (!plan->sf_valid || plan->sf_ptrs[0] != sf_a || plan->sf_ptrs[1] != sf_b) {
+        plan->sf_valid = false;
+        if (!encode_sf_map(&plan->sf_maps[0], sf_a, d.M, kq, d.batch, d.stride_sa, chunks) ||
+            !encode_sf_map(&plan->sf_maps[1], sf_b, d.N, kq, d.batch, d.stride_sb, chunks)) {
+            g_last_cuda_error = (int)cudaErrorInvalidValue;
+            return GEMM_ERR_CUDA;
+        }
+        plan->sf_ptrs[0] = sf_a;
+        plan->sf_ptrs[1] = sf_b;
+        plan->sf_valid = true;
+    }
+    dgb::MxParams q;
+    std::memset(&q, 0, sizeof(q));
+    PersistentParams& p = q.base;
+    p.tmap_a = plan->maps[0];
+    p.tmap_b = plan->maps[1];
+    p.tmap_d = plan->maps[2];
+    p.status = plan->status;
+    p.M = (int32_t)d.M; p.N = (int32_t)d.N; p.K = (int32_t)d.K; p.batch = (int32_t)d.batch;
+    fill_schedule(d, info, p);              // K blocks of info.tile_k elements (one 128-byte atom)
+    p.tile_n = info.tile_n;
+    p.stages = info.stages;
+    p.tmem_cols = info.tmem_cols;
+    p.tmem_stages = 1;
+    p.batched = d.batch > 1 ? 1 : 0;
+    p.tile_k = 128;                         // the producers' K coordinate counts bytes
+    p.k_atoms = 1;
+    p.mn_box_elems = 128;
+    // element formats: mxf8f6f4 0 = E4M3, 1 = E5M2; mxf4 / mxf4nvf4 1 = E2M1; scales UE8M0 (MX) or UE4M3 (NV)
+    const uint32_t fa = fp4 ? 1u : (d.dtype_a == GEMM_E5M2 ? 1u : 0u);
+    const uint32_t fb = fp4 ? 1u : (d.dtype_b == GEMM_E5M2 ? 1u : 0u);
+    p.idesc = dgb::make_idesc_block_scaled(fa, fb, (uint32_t)info.tile_m, (uint32_t)info.tile_n, nv ? 0u : 1u);
+    p.stage_bytes_a = 128u * 128u;
+    p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * 128);
+    p.flags = d.flags;
+    p.timeout_ns = d.wait_timeout_ns;
+    p.l2_hints = (d.batch == 1 && p.num_k_blocks >= 8 && !(d.flags & GEMM_FLAG_NO_L2_HINTS))
+                     ? (dgb::kHintKeepA | dgb::kHintStreamD) : 0u;
+    p.d_ptr = D;
+    p.ldd = d.ldd;
+    p.stride_d = d.stride_d;
+    q.tmap_sfa = plan->sf_maps[0];
+    q.tmap_sfb = plan->sf_maps[1];
+    q.tensor_scales = nv ? tensor_scales : nullptr;
+    q.chunks = chunks;
+    q.sf_stage_bytes = (uint32_t)(3 * chunks * 512);
+    q.sf_ring_offset = (uint32_t)info.stages * (p.stage_bytes_a + p.stage_bytes_b);
+    e = dgb::launch_mx(q, mx_kind(d), cg, d.dtype_d, info.grid, (size_t)info.smem_bytes, stream);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
 // Panels for gemm_run_host: rows of A and D (one batch entry), or batch
 // entries; each panel large enough that its GEMM keeps the GPU busy.
 static int host_panels(const gemm_desc_t& d, int64_t* unit0) {
@@ -920,6 +1146,7 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, vo
     if (!plan) return GEMM_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const gemm_desc_t& d = plan->desc;
+    if (hw_scaled(d.scale_mode)) return GEMM_ERR_UNSUPPORTED;
     if (d.M == 0 || d.N == 0 || d.batch == 0) return GEMM_OK;
     if (!hD || !dD) return GEMM_ERR_INVALID_ARG;
     const bool ka = d.major_a == GEMM_K_MAJOR, kb = d.major_b == GEMM_K_MAJOR;
@@ -1076,6 +1303,7 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
     Resolved r;
     gemm_status_t s = resolve(desc, &r);
     if (s != GEMM_OK) return s;
+    if (hw_scaled(r.d.scale_mode)) return GEMM_ERR_UNSUPPORTED;
     // The only device memory the kernels use beyond A, B, D and the scales is
     // their error record; it must fit the static array.
     if (sizeof(gemm_device_error_t) > sizeof(g_noalloc_scratch)) return GEMM_ERR_RESOURCES;

@@ -99,14 +99,14 @@ MX_EMAX = {"e4m3": 8, "e5m2": 15, "e2m1": 2}     # exponent of each element form
 
 def e2m1_codes(x: torch.Tensor) -> torch.Tensor:
     """Round fp32 values to the nearest E2M1 value (ties to the even code, beyond
-    6 saturated); returns the 4-bit codes as uint8."""
-    grid = torch.tensor(E2M1_GRID, dtype=torch.float32)
+    6 saturated); returns the 4-bit codes as uint8.  The values are spaced 0.5
+    below 2, 1 in [2, 4) and 2 in [4, 6], and codes count along them, so
+    round-half-to-even within each binade picks the nearest code and, at a
+    tie, the even one."""
     a = x.abs().clamp(max=6.0)
-    lo = (torch.searchsorted(grid, a, right=True) - 1).clamp(0, 7)
-    hi = (lo + 1).clamp(max=7)
-    dlo, dhi = a - grid[lo], grid[hi] - a
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0) & (hi != lo))
-    idx = torch.where(pick_hi, hi, lo)
+    idx = torch.where(a < 2.0, torch.round(a * 2.0),
+                      torch.where(a < 4.0, 4.0 + torch.round(a - 2.0), 6.0 + torch.round((a - 4.0) * 0.5)))
+    idx = idx.to(torch.int64)
     sign = ((x < 0) & (idx > 0)).to(torch.int64)
     return (idx | (sign << 3)).to(torch.uint8)
 

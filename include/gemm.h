@@ -17,9 +17,28 @@
  *   A, K-major  : A[b*stride_a + m*lda + k]    A, MN-major : A[b*stride_a + k*lda + m]
  *   B, K-major  : B[b*stride_b + n*ldb + k]    B, MN-major : B[b*stride_b + k*ldb + n]
  *   D (row-major): D[b*stride_d + m*ldd + n]
- *   scale_a     : scale_a[b*stride_sa + m*ld_sa + k/128]           (block-scaled only)
- *   scale_b     : scale_b[b*stride_sb + (n/128)*ld_sb + k/128]     (block-scaled only)
+ *   scale_a     : scale_a[b*stride_sa + m*ld_sa + k/128]           (fp32 block scales only)
+ *   scale_b     : scale_b[b*stride_sb + (n/128)*ld_sb + k/128]     (fp32 block scales only)
  * "row-major A, column-major B" in BLAS terms is K-major A and K-major B (TN).
+ * GEMM_E2M1 elements are packed two per byte, element k of a row in the low
+ * nibble of byte k/2 when k is even and in the high nibble when k is odd;
+ * leading dims and batch strides still count elements.
+ *
+ * Hardware block scaling (GEMM_SCALE_MX_E8M0_32, GEMM_SCALE_NV_E4M3_16; the
+ * formats of "Hopper and Blackwell GEMM", concept "FP8 and FP4, with block
+ * scaling"): each row of A and each row of B (K-major) is cut along K into
+ * blocks of V elements (V = 32 for MX, 16 for NV), every block with one scale
+ * byte (MX: E8M0, 2^(e-127), 0xFF is NaN; NV: E4M3 with sign bit 0).  For a
+ * matrix with R rows and KB = ceil(K/V) scale columns the scale bytes are
+ * tiled as the tensor core reads them ("TMEM -- the accumulator's new home",
+ * section "Block-scaled MMA": lane = row mod 32, column = row / 32): 512-byte
+ * tiles of 128 rows x 4 scale columns,
+ *   tile (r/128, kb/4) at byte  ((r/128) * ceil(KB/4) + kb/4) * 512
+ *   inside a tile      at byte  (r mod 32) * 16 + ((r/32) mod 4) * 4 + kb mod 4
+ * from the batch entry's start (stride_sa / stride_sb bytes apart; 0 = packed,
+ * ceil(R/128) * ceil(KB/4) * 512).  Entries past R or KB must hold finite
+ * codes (they meet zero-filled operands).  NV additionally multiplies D by
+ * one fp32 scale per tensor, tA * tB.
  *
  * Ownership: the caller owns every device buffer and the stream; the library
  * never frees or retains them past the call that uses them.  A plan owns its
@@ -62,16 +81,23 @@ typedef enum {
 
 /* Element types.  GEMM_TF32 is fp32 storage multiplied at tf32 precision (the
  * tensor core reads the top 19 bits of each fp32 value); GEMM_F32 is an output type. */
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_F32 = 3, GEMM_E5M2 = 4, GEMM_TF32 = 5 } gemm_dtype_t;
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_F32 = 3, GEMM_E5M2 = 4, GEMM_TF32 = 5,
+               GEMM_E2M1 = 6 } gemm_dtype_t;
 typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
-typedef enum { GEMM_SCALE_NONE = 0, GEMM_SCALE_BLOCK_1x128_128x128 = 1 } gemm_scale_mode_t;
+typedef enum {
+    GEMM_SCALE_NONE = 0,
+    GEMM_SCALE_BLOCK_1x128_128x128 = 1,  /* fp32 scale per 1x128 block of A and 128x128 block of B (gemm_run) */
+    GEMM_SCALE_MX_E8M0_32 = 2,           /* MXFP8 (E4M3/E5M2) or MXFP4 (E2M1): E8M0 per 32, tiled (gemm_run_mx) */
+    GEMM_SCALE_NV_E4M3_16 = 3            /* NVFP4 (E2M1): E4M3 per 16, tiled, times fp32 tA * tB (gemm_run_mx) */
+} gemm_scale_mode_t;
 
 /* Kernel families a plan can select. */
 typedef enum {
     GEMM_KERNEL_SINGLE_CTA = 1,   /* one CTA per problem, threads stage operands (small problems) */
     GEMM_KERNEL_PERSISTENT = 2,   /* warp-specialised persistent TMA/tcgen05 pipeline */
     GEMM_KERNEL_FP8_BLOCK = 3,    /* persistent pipeline with per-block scale promotion */
-    GEMM_KERNEL_ZERO_FILL = 4     /* K == 0: D is written with zeros */
+    GEMM_KERNEL_ZERO_FILL = 4,    /* K == 0: D is written with zeros */
+    GEMM_KERNEL_MX = 5            /* persistent pipeline with hardware block-scaled MMA (MX / NVFP4) */
 } gemm_kernel_t;
 
 /* gemm_desc_t.flags */
@@ -96,19 +122,20 @@ typedef enum {
 typedef struct {
     int64_t M, N, K;        /* D is M x N per batch entry; K is the contraction length */
     int64_t batch;          /* number of independent problems (>= 1; 0 = no-op) */
-    int32_t dtype_a, dtype_b;   /* gemm_dtype_t: F16+F16, BF16+BF16, TF32+TF32 (K-major), or any pair of
-                                   E4M3/E5M2 (block-scaled) */
+    int32_t dtype_a, dtype_b;   /* gemm_dtype_t: F16+F16, BF16+BF16, TF32+TF32 (K-major), any pair of
+                                   E4M3/E5M2 (fp32 block scales or MX), E2M1+E2M1 (MX or NV, K-major) */
     int32_t dtype_d;            /* gemm_dtype_t: F32, BF16 or F16 */
     int32_t major_a, major_b;   /* gemm_major_t */
-    int32_t scale_mode;         /* gemm_scale_mode_t; BLOCK requires E4M3 inputs */
+    int32_t scale_mode;         /* gemm_scale_mode_t; BLOCK and MX require 8-bit or E2M1 inputs as listed */
     int64_t lda, ldb, ldd;      /* leading dims in elements; 0 = packed (K or M/N, and N for D) */
     int64_t stride_a, stride_b, stride_d;  /* elements between batch entries; 0 = packed */
-    int64_t ld_sa, ld_sb;       /* scale leading dims in floats; 0 = ceil(K/128) */
-    int64_t stride_sa, stride_sb;  /* floats between batch entries of the scales; 0 = packed */
+    int64_t ld_sa, ld_sb;       /* fp32 block scales: leading dims in floats, 0 = ceil(K/128); MX/NV: must be 0 */
+    int64_t stride_sa, stride_sb;  /* between batch entries of the scales: floats (fp32 block scales) or bytes
+                                      (MX/NV tiles); 0 = packed */
     uint32_t flags;             /* GEMM_FLAG_* */
     int32_t tile_n;             /* N extent of one output tile: a multiple of 16 in 16..256, or 512 (16-bit/tf32
                                    K-major operands: two N = 256 MMAs per K step, one 512-column accumulator);
-                                   block-scaled fp8: 128 or 256; 0 = planner */
+                                   block-scaled fp8: 128 or 256; MX/NV: 256; 0 = planner */
     int32_t stages;             /* shared-memory ring depth (2..16); 0 = planner */
     int32_t max_ctas;           /* cap on persistent CTAs; 0 = all SMs */
     uint64_t wait_timeout_ns;   /* bound on every device-side wait; 0 = 2 s */
@@ -233,11 +260,30 @@ gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_
  * correct.  Launches of one plan must be ordered (one stream, or streams
  * joined by events): concurrent launches would share its status record,
  * stream-K workspace and launch counter.
- * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT or GEMM_ERR_CUDA.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (also for an MX / NV plan, which
+ * gemm_run_mx runs), GEMM_ERR_ALIGNMENT or GEMM_ERR_CUDA.
  * Device-side wait expiry is not visible here; see gemm_sync_status.
  */
 gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
                        const float* scale_a, const float* scale_b, gemm_stream_t stream);
+
+/*
+ * gemm_run_mx -- enqueue D = tA*tB * (A . SA) * (B . SB)^T on `stream` for a
+ * plan whose scale_mode is GEMM_SCALE_MX_E8M0_32 or GEMM_SCALE_NV_E4M3_16
+ * (kernel GEMM_KERNEL_MX): the tensor core applies the block scales inside
+ * tcgen05.mma (.kind::mxf8f6f4 for 8-bit elements, .kind::mxf4 for MXFP4,
+ * .kind::mxf4nvf4 for NVFP4), fp32 accumulation, one rounding to D's type.
+ * A, B, D: device pointers laid out as at the top of this file (K-major A and
+ * B; E2M1 rows a multiple of 32 elements apart, K even).  sf_a, sf_b: device
+ * pointers to the tiled scale bytes (16-byte aligned).  tensor_scales: NV: a
+ * device pointer to two fp32 values {tA, tB}, read by the kernel when it runs;
+ * MX: NULL.  Asynchronous and stream-ordered like gemm_run.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (a plan of another kind, a missing or
+ * superfluous pointer), GEMM_ERR_ALIGNMENT or GEMM_ERR_CUDA; device-side wait
+ * expiry is reported by gemm_sync_status.
+ */
+gemm_status_t gemm_run_mx(gemm_plan_t plan, const void* A, const void* B, void* D, const void* sf_a,
+                          const void* sf_b, const float* tensor_scales, gemm_stream_t stream);
 
 /*
  * gemm_run_host -- the same product for operands that live in host memory.
@@ -258,7 +304,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
  * plans are created on the first call and freed by gemm_plan_destroy; calls
  * on one plan must not run concurrently from several host threads.
  * The call returns once the work is enqueued; synchronise `stream` before
- * reading hD.
+ * reading hD.  MX / NV plans are not offered here (GEMM_ERR_UNSUPPORTED).
  */
 gemm_status_t gemm_run_host(gemm_plan_t plan, const void* hA, const void* hB, void* hD,
                             const float* hscale_a, const float* hscale_b,
@@ -298,7 +344,7 @@ gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream, gemm_devi
  * status_out: NULL returns once the work is enqueued; otherwise the call
  * synchronises `stream`, copies the record into *status_out and returns its
  * code (GEMM_OK or GEMM_ERR_TIMEOUT).  Other returns: the codes of
- * gemm_plan_create and gemm_run.
+ * gemm_plan_create and gemm_run (MX / NV problems: GEMM_ERR_UNSUPPORTED).
  */
 gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const void* B, void* D,
                                const float* scale_a, const float* scale_b, gemm_stream_t stream,

@@ -1,0 +1,155 @@
+"""GPU parity of the hardware block-scaled path (MXFP8, MXFP4, NVFP4) against
+the CPU oracle.
+
+"Hopper and Blackwell GEMM", concept "FP8 and FP4, with block scaling": the
+tensor core multiplies each block of a row of A and of B by its own scale
+inside tcgen05.mma (.kind::mxf8f6f4, .kind::mxf4, .kind::mxf4nvf4), the
+scales read from tensor memory after a tcgen05.cp from shared memory ("TMEM
+-- the accumulator's new home", section "Block-scaled MMA").  Both sides read
+the same element and scale bytes; the oracle sums the exact products in fp64,
+the GPU in fp32.  Integer-valued elements with power-of-two scales keep every
+sum exact, so those runs must match bit for bit; quantised N(0,1) inputs must
+stay within 2e-3 of sum |a||b| (the products themselves are exact on both
+sides, so only fp32 accumulation separates them: the 16-bit inputs' bound).
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_blackwell_gb300 as dg
+from dense_gemm_blackwell_gb300 import inputs
+import oracle
+from parity import TOL_16BIT, compare, dump_on_failure
+
+pytestmark = pytest.mark.gpu
+
+TDT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+CODE = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32}
+IN = {"e4m3": dg.GEMM_E4M3, "e5m2": dg.GEMM_E5M2, "e2m1": dg.GEMM_E2M1}
+MODE = {"mx": dg.GEMM_SCALE_MX_E8M0_32, "nv": dg.GEMM_SCALE_NV_E4M3_16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dg.build()
+    torch.cuda.init()
+
+
+def run_mx(prob, out, **kw):
+    wl = prob.wl
+    mode = wl.extra["scale_mode"]
+    D = torch.full((wl.M, wl.N), float("nan"), dtype=TDT[out], device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=IN[wl.dtype_in], dtype_b=IN[wl.extra["dtype_b"]],
+                        dtype_d=CODE[out], scale_mode=MODE[mode], **kw)
+    ts = torch.tensor(prob.tensor_scales, dtype=torch.float32, device="cuda") if mode == "nv" else None
+    with dg.Plan(desc) as plan:
+        plan.run_mx(prob.A.cuda(), prob.B.cuda(), D, prob.scale_a.cuda(), prob.scale_b.cuda(), ts)
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, (dg.gemm_status_string(s), rec.role, rec.stage, rec.tile)
+        info = plan.info.as_dict()
+    assert info["kernel"] == dg.GEMM_KERNEL_MX
+    return D, info
+
+
+def oracle_mx(prob, rows=None):
+    wl = prob.wl
+    return oracle.gemm_rows(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a=wl.dtype_in,
+                            dtype_b=wl.extra["dtype_b"], scale_a=prob.scale_a, scale_b=prob.scale_b,
+                            scale_mode=wl.extra["scale_mode"], tensor_scales=prob.tensor_scales, rows=rows)
+
+
+def check(prob, out, exact, **kw):
+    D, info = run_mx(prob, out, **kw)
+    dref, s = oracle_mx(prob)
+    got = D.double().cpu().numpy()
+    r = compare(got, dref[0], s[0], out, TOL_16BIT, exact=exact)
+    if not r["ok"]:
+        dump_on_failure("mx_%s_%s_cg%d" % (prob.wl.name, out, info["cta_group"]), got=got, dref=dref[0], sabs=s[0])
+    assert r["ok"], (r, info)
+    return info
+
+
+# ragged M, N and K in every case: a partial 128-row block, a partial tile
+# column, a K tail inside the last 128-byte atom (partial scale blocks)
+SMALL = {"mxfp8_8192": dict(M=300, N=520, K=400), "mxfp4_8192": dict(M=300, N=520, K=416),
+         "nvfp4_8192": dict(M=300, N=520, K=448)}
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+def test_block_scaled_integers_bit_exact(name, cg_flag):
+    prob = inputs.make(name, dist="ints", seed=51, **SMALL[name])
+    info = check(prob, "f32", exact=True, flags=cg_flag)
+    assert info["cta_group"] == (1 if cg_flag == dg.GEMM_FLAG_CTA_GROUP_1 else 2)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+def test_block_scaled_integers_16bit_out(name, out):
+    prob = inputs.make(name, dist="ints", seed=52, **SMALL[name])
+    check(prob, out, exact=True)
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+def test_block_scaled_quantised_normal(name, cg_flag):
+    prob = inputs.make(name, seed=53, **SMALL[name])
+    check(prob, "bf16", exact=False, flags=cg_flag)
+
+
+def test_mxfp8_e5m2_pairing_bit_exact():
+    prob = inputs.make("mxfp8_8192", dist="ints", seed=54, dtype_b="e5m2", **SMALL["mxfp8_8192"])
+    check(prob, "f32", exact=True)
+
+
+def test_block_scaled_many_tiles_few_ctas():
+    """More tiles than clusters: the single accumulator and the scale slots cycle."""
+    prob = inputs.make("mxfp8_8192", dist="ints", seed=55, M=1024, N=1280, K=640)
+    check(prob, "f32", exact=True, max_ctas=6, flags=dg.GEMM_FLAG_CTA_GROUP_2)
+    prob = inputs.make("nvfp4_8192", dist="ints", seed=56, M=1024, N=1280, K=768)
+    check(prob, "f32", exact=True, max_ctas=5, flags=dg.GEMM_FLAG_CTA_GROUP_1)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+def test_full_size_integers_bit_exact(name):
+    """The benchmark's plan at 8192^3 on seeded rows plus both edge rows of every 128-row block."""
+    prob = inputs.make(name, dist="ints")
+    D, info = run_mx(prob, "bf16")
+    assert (info["cta_group"], info["tile_n"], info["grid"]) == (2, 256, 152), info
+    rows = inputs.sample_rows(prob.wl.M, 1, n_random=48, seed=5, tile_m=128)
+    dref, s = oracle_mx(prob, rows)
+    got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref, s, "bf16", TOL_16BIT, exact=True)
+    assert r["ok"], (name, r, info)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+def test_full_size_quantised_normal_sampled(name):
+    prob = inputs.make(name)
+    D, info = run_mx(prob, "bf16")
+    rows = inputs.sample_rows(prob.wl.M, 1, n_random=32, seed=6, tile_m=256)
+    dref, s = oracle_mx(prob, rows)
+    got = D[torch.tensor(rows, device="cuda")].double().cpu().numpy()
+    r = compare(got, dref, s, "bf16", TOL_16BIT)
+    assert r["ok"], (name, r, info)
+
+
+def test_wrong_entry_points_are_refused():
+    prob = inputs.make("mxfp8_8192", dist="ints", seed=57, M=256, N=256, K=256)
+    desc = dg.make_desc(256, 256, 256, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_F32,
+                        scale_mode=dg.GEMM_SCALE_MX_E8M0_32)
+    A, B, sa, sb = prob.A.cuda(), prob.B.cuda(), prob.scale_a.cuda(), prob.scale_b.cuda()
+    D = torch.zeros(256, 256, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    with dg.Plan(desc) as plan:
+        assert dg.gemm_run(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), sa.data_ptr(), sb.data_ptr(),
+                           stream) == dg.GEMM_ERR_INVALID_ARG
+        ts = torch.ones(2, device="cuda")
+        assert dg.gemm_run_mx(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), sa.data_ptr(), sb.data_ptr(),
+                              ts.data_ptr(), stream) == dg.GEMM_ERR_INVALID_ARG   # tensor scales are NVFP4's
+        assert dg.gemm_run_mx(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), sa.data_ptr() + 8,
+                              sb.data_ptr(), None, stream) == dg.GEMM_ERR_ALIGNMENT
+    assert dg.gemm_run_noalloc(desc, A.data_ptr(), B.data_ptr(), D.data_ptr(), None, None, stream,
+                               None) == dg.GEMM_ERR_UNSUPPORTED
