@@ -3,6 +3,7 @@
 fp32 output, on one GB300 -- TFLOP/s and fraction of the measured dense bf16 peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-other-workloads]
 
 One step = one gemm_run of the whole product (host planning of the tensor maps
 + one persistent kernel launch).  Inputs are seeded synthetic matrices (U[-1,1])
@@ -10,6 +11,11 @@ resident in HBM; the working set (A 134 MB + B 134 MB + D 268 MB) is larger than
 the 129 MB L2, so no flush is inserted between steps.  With N > 1 (torchrun),
 every rank runs its own replica of the product on its own GPU (no collective on
 the data path); the elapsed time is the maximum over ranks.
+
+After the headline, the same run times every other workload of the suite
+(single-CTA example, 4096^3, batched 512 x 256^3, fp32-block-scaled e4m3,
+MXFP8, MXFP4, NVFP4) with its own launches, CUDA events, clock samples and
+roofline, reported under "other_workloads" on the same JSON line.
 
 --impl reference times the CPU oracle (the plain fp64 triple loop) on this
 host's cores on a bounded sample of the same workload (rank 0 only).
@@ -34,17 +40,124 @@ WORKLOAD = "square8192_bf16"
 METRIC = "GEMM TFLOP/s (bf16 in, fp32 acc, 8192^3) and fraction of GB300 dense peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
-PROFILE = os.path.join(ROOT, "profiles", "persistent_pair_square8192_bf16_f32.md")
-# everything that decides what the headline kernel does: its code, its work
-# schedule and the host code that plans and launches it
-KERNEL_SOURCES = ["dense_gemm_blackwell_gb300/csrc/kernels_persistent.cu",
-                  "dense_gemm_blackwell_gb300/csrc/pipeline.cuh",
-                  "dense_gemm_blackwell_gb300/csrc/units.cuh",
-                  "dense_gemm_blackwell_gb300/csrc/ptx.cuh",
-                  "dense_gemm_blackwell_gb300/csrc/common.cuh",
-                  "dense_gemm_blackwell_gb300/csrc/launch.h",
-                  "dense_gemm_blackwell_gb300/csrc/gemm_api.cu",
-                  "include/gemm.h"]
+# tcgen05.mma throughput per SM per cycle, measured on GB300 with a probe that
+# issues M128 N256 MMAs back to back on every SM: 128 cycles per instruction
+# for kind::f16 (K16), kind::f8f6f4 / mxf8f6f4 (K32) and kind::mxf4 /
+# mxf4nvf4 (K64) alike.  (The 4-bit rate is 4x bf16, not the 6x of GB300's
+# nominal dense figures; the roofline "peak" keeps the nominal ratio.)
+MMA_FLOP_PER_CYCLE_SM = {"bf16": 8192.0, "fp8": 16384.0, "fp4": 32768.0}
+# Files that decide what each kernel does: its code, its work schedule, the host
+# code that plans and launches it.  A profile's DRAM figures count only while
+# these hash to the value the profile records.
+_SHARED = ["dense_gemm_blackwell_gb300/csrc/pipeline.cuh", "dense_gemm_blackwell_gb300/csrc/units.cuh",
+           "dense_gemm_blackwell_gb300/csrc/ptx.cuh", "dense_gemm_blackwell_gb300/csrc/common.cuh",
+           "dense_gemm_blackwell_gb300/csrc/launch.h", "dense_gemm_blackwell_gb300/csrc/gemm_api.cu",
+           "include/gemm.h"]
+SOURCES = {
+    "persistent": ["dense_gemm_blackwell_gb300/csrc/kernels_persistent.cu"] + _SHARED,
+    "single": ["dense_gemm_blackwell_gb300/csrc/kernels_single.cu"] + _SHARED,
+    "fp8_block": ["dense_gemm_blackwell_gb300/csrc/kernels_fp8.cu"] + _SHARED,
+    "mx": ["dense_gemm_blackwell_gb300/csrc/kernels_mx.cu", "dense_gemm_blackwell_gb300/csrc/mx_ptx.cuh"] + _SHARED,
+}
+KERNEL_SOURCES = SOURCES["persistent"]
+
+
+def _prof(name):
+    return os.path.join(ROOT, "profiles", name)
+
+
+# Per-workload metric, roofline bound, peak (a multiple of the measured bf16
+# peak: the nominal dtype ratio), kernel family and committed ncu summary.
+WORKLOAD_INFO = {
+    "square8192_bf16": dict(metric=METRIC, unit=UNIT, bound="tensor", peak_ratio=1.0, rate="bf16",
+                            kernel="persistent", profile=_prof("persistent_pair_square8192_bf16_f32.md"),
+                            text="D = A*B^T, M=N=K=8192, bf16 TN, fp32 accumulate, fp32 out"),
+    "square4096_bf16": dict(metric="GEMM TFLOP/s (bf16 in, fp32 acc, bf16 out, 4096^3)", unit=UNIT,
+                            bound="tensor", peak_ratio=1.0, rate="bf16", kernel="persistent",
+                            profile=_prof("persistent_pair_square4096_bf16.md"),
+                            text="D = A*B^T, M=N=K=4096, bf16 TN, fp32 accumulate, bf16 out"),
+    "batched256_f16": dict(metric="batched GEMM GB/s (512 x 256^3, f16 in/out, fp32 acc)", unit="GB/s",
+                           bound="hbm", peak_ratio=1.0, rate="bf16", kernel="persistent",
+                           profile=_prof("persistent_batched256_f16.md"),
+                           text="512 independent D = A*B^T of 256^3, f16 TN, fp32 accumulate, f16 out"),
+    "fp8_block8192": dict(metric="GEMM TFLOP/s (e4m3 block-scaled in, fp32 acc, bf16 out, 8192^3)", unit=UNIT,
+                          bound="tensor", peak_ratio=2.0, rate="fp8", kernel="fp8_block",
+                          profile=_prof("fp8_block_square8192_e4m3_bf16.md"),
+                          text="D = (qA sA)(qB sB)^T, 8192^3, e4m3 TN, fp32 scales 1x128 / 128x128, bf16 out"),
+    "mxfp8_8192": dict(metric="GEMM TFLOP/s (MXFP8: e4m3 in, E8M0 per 32, fp32 acc, bf16 out, 8192^3)", unit=UNIT,
+                       bound="tensor", peak_ratio=2.0, rate="fp8", kernel="mx",
+                       profile=_prof("mx_pair_mxfp8_8192_bf16.md"),
+                       text="D = (qA . sA)(qB . sB)^T, 8192^3, e4m3 TN, E8M0 scale per 32 K elements "
+                            "(tcgen05 block scaling), bf16 out"),
+    "mxfp4_8192": dict(metric="GEMM TFLOP/s (MXFP4: e2m1 in, E8M0 per 32, fp32 acc, bf16 out, 8192^3)", unit=UNIT,
+                       bound="tensor", peak_ratio=6.0, rate="fp4", kernel="mx",
+                       profile=_prof("mx_pair_mxfp4_8192_bf16.md"),
+                       text="D = (qA . sA)(qB . sB)^T, 8192^3, e2m1 TN (packed), E8M0 scale per 32 K elements "
+                            "(tcgen05 block scaling), bf16 out"),
+    "nvfp4_8192": dict(metric="GEMM TFLOP/s (NVFP4: e2m1 in, E4M3 per 16 + fp32 per tensor, fp32 acc, bf16 out, "
+                              "8192^3)", unit=UNIT, bound="tensor", peak_ratio=6.0, rate="fp4", kernel="mx",
+                       profile=_prof("mx_pair_nvfp4_8192_bf16.md"),
+                       text="D = tA tB (qA . sA)(qB . sB)^T, 8192^3, e2m1 TN (packed), E4M3 scale per 16 K elements "
+                            "(tcgen05 block scaling), bf16 out"),
+    "single_cta": dict(metric="single-CTA GEMM latency (128x64x64 f16 -> f32)", unit="us/launch",
+                       bound="latency", peak_ratio=1.0, rate="bf16", kernel="single",
+                       profile=_prof("single_cta_128x64x64_f16.md"),
+                       text="Out = A @ B.T, A 128x64, B 64x64 f16, fp32 out, one CTA"),
+}
+# the other workloads timed after the headline, with launches per timed region
+OTHER_WORKLOADS = [("single_cta", 2000), ("square4096_bf16", 400), ("batched256_f16", 600),
+                   ("fp8_block8192", 100), ("mxfp8_8192", 100), ("mxfp4_8192", 200), ("nvfp4_8192", 200)]
+
+
+def kernel_source_hash(name: str = WORKLOAD) -> str:
+    h = hashlib.sha256()
+    for rel in SOURCES[WORKLOAD_INFO[name]["kernel"]]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str = WORKLOAD):
+    """DRAM bytes per launch from the workload's committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    try:
+        text = open(WORKLOAD_INFO[name]["profile"]).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash(name):
+        return None
+    return float(m_tr.group(1))
+
+
+def config_for(name: str, world: int = 1) -> dict:
+    """The `config` object of a workload's line (identical in both arms)."""
+    from dense_gemm_blackwell_gb300 import inputs
+    wl = inputs.WORKLOADS[name]
+    winfo = WORKLOAD_INFO[name]
+    ws = working_set_bytes(name)
+    return {"workload": "%s: %s" % (name, winfo["text"]), "M": wl.M, "N": wl.N, "K": wl.K, "batch": wl.batch,
+            "inputs": "%s seed %d" % (wl.dist, wl.seed),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": ("no flush: working set %.0f MB > 129 MB L2" % (ws / 1e6)) if ws > 129e6
+            else "no flush: working set %.1f MB fits L2 (L2-warm)" % (ws / 1e6)}
+
+
+def working_set_bytes(name: str) -> float:
+    """Algorithmic bytes of one launch: A, B, D and any scales, once each."""
+    from dense_gemm_blackwell_gb300 import inputs
+    wl = inputs.WORKLOADS[name]
+    bits = {"f16": 16, "bf16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}
+    total = (wl.M + wl.N) * wl.K * wl.batch * bits[wl.dtype_in] / 8 + wl.M * wl.N * wl.batch * bits[wl.dtype_out] / 8
+    mode = wl.extra.get("scale_mode")
+    if wl.block_scaled:
+        total += 4 * (wl.M * -(-wl.K // 128) + -(-wl.N // 128) * -(-wl.K // 128))
+    elif mode in ("mx", "nv"):
+        v = 32 if mode == "mx" else 16
+        kq = -(-(-(-wl.K // v)) // 4)
+        total += 512 * kq * (-(-wl.M // 128) + -(-wl.N // 128)) + (8 if mode == "nv" else 0)
+    return float(total)
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -77,28 +190,6 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured HBM copy (MEASURED_PEAKS.json)"
     except Exception:
         return 6800.0, "fallback 6.8 TB/s"
-
-
-def kernel_source_hash() -> str:
-    h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
-
-
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
-    try:
-        text = open(PROFILE).read()
-    except OSError:
-        return None
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
-        return None
-    return float(m_tr.group(1))
 
 
 class ClockSampler:
@@ -169,8 +260,12 @@ def _oracle_rows(prob, rows, ncols=None):
     wl = prob.wl
     N = wl.N if ncols is None else ncols
     B = prob.B if ncols is None else (prob.B[..., :N, :] if wl.batch == 1 else prob.B[:, :N, :]).contiguous()
-    kw = dict(M=wl.M, N=N, K=wl.K, batch=wl.batch, dtype_a=wl.dtype_in, dtype_b=wl.dtype_in)
-    if wl.block_scaled:
+    kw = dict(M=wl.M, N=N, K=wl.K, batch=wl.batch, dtype_a=wl.dtype_in, dtype_b=wl.extra.get("dtype_b", wl.dtype_in))
+    if wl.extra.get("scale_mode") in ("mx", "nv"):
+        # tiled scales: a row's scales sit where its row block puts them, whatever N is
+        kw.update(scale_a=prob.scale_a, scale_b=prob.scale_b, scale_mode=wl.extra["scale_mode"],
+                  tensor_scales=prob.tensor_scales)
+    elif wl.block_scaled:
         sb = prob.scale_b.numpy()[: (N + 127) // 128]
         kw.update(scale_a=prob.scale_a.numpy(), scale_b=sb, ld_sb=prob.scale_b.shape[1])
     oracle.gemm_rows(prob.A, B, rows=rows, **kw)
@@ -195,8 +290,7 @@ def cpu_oracle_sample(seconds_target: float, prob=None, unit=UNIT):
     desc = "%d of %d rows of D (all %d columns, K=%d) of %s, fp64 oracle" % (rows, wl.M * wl.batch, wl.N, wl.K, wl.name)
     if unit == "GB/s":
         frac = rows / float(wl.M * wl.batch)
-        total = sum(t_.numel() * t_.element_size() for t_ in (prob.A, prob.B)) + wl.M * wl.N * wl.batch * 2
-        return total * frac / dt / 1e9, oracle.num_threads(), desc, dt
+        return working_set_bytes(wl.name) * frac / dt / 1e9, oracle.num_threads(), desc, dt
     if unit == "us/launch":
         return dt * 1e6 * (wl.M * wl.batch) / rows, oracle.num_threads(), desc, dt
     return flops / dt / 1e12, oracle.num_threads(), desc, dt
@@ -233,8 +327,7 @@ def run_reference(args):
     frac = rows * ncols / float(wl.M * wl.batch * wl.N)
     work_s = dt / max(args.steps, 1) / frac          # seconds for the whole product at this rate
     if winfo["unit"] == "GB/s":
-        total = sum(t_.numel() * t_.element_size() for t_ in (prob.A, prob.B)) + wl.M * wl.N * wl.batch * 2
-        value = total / work_s / 1e9
+        value = working_set_bytes(args.workload) / work_s / 1e9
     elif winfo["unit"] == "us/launch":
         value = work_s * 1e6
     else:
@@ -247,8 +340,7 @@ def run_reference(args):
         "ms_per_step": dt * 1e3 / max(args.steps, 1),
         "higher_is_better": winfo["unit"] != "us/launch", "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s: %s" % (args.workload, winfo["text"]), "M": wl.M, "N": wl.N, "K": wl.K,
-                   "batch": wl.batch, "inputs": "%s seed %d" % (wl.dist, wl.seed)},
+        "config": config_for(args.workload, args.gpus),
         "cpu_baseline": {"value": value, "unit": winfo["unit"], "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": winfo["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -257,23 +349,162 @@ def run_reference(args):
     return 0
 
 
-# Per-workload metric and roofline bound.  The default workload is the headline.
-WORKLOAD_INFO = {
-    "square8192_bf16": dict(metric=METRIC, unit=UNIT, bound="tensor", peak_ratio=1.0,
-                            text="D = A*B^T, M=N=K=8192, bf16 TN, fp32 accumulate, fp32 out"),
-    "square4096_bf16": dict(metric="GEMM TFLOP/s (bf16 in, fp32 acc, bf16 out, 4096^3)", unit=UNIT,
-                            bound="tensor", peak_ratio=1.0,
-                            text="D = A*B^T, M=N=K=4096, bf16 TN, fp32 accumulate, bf16 out"),
-    "batched256_f16": dict(metric="batched GEMM GB/s (512 x 256^3, f16 in/out, fp32 acc)", unit="GB/s",
-                           bound="hbm", peak_ratio=1.0,
-                           text="512 independent D = A*B^T of 256^3, f16 TN, fp32 accumulate, f16 out"),
-    "fp8_block8192": dict(metric="GEMM TFLOP/s (e4m3 block-scaled in, fp32 acc, bf16 out, 8192^3)", unit=UNIT,
-                          bound="tensor", peak_ratio=2.0,
-                          text="D = (qA sA)(qB sB)^T, 8192^3, e4m3 TN, fp32 scales 1x128 / 128x128, bf16 out"),
-    "single_cta": dict(metric="single-CTA GEMM latency (128x64x64 f16 -> f32)", unit="us/launch",
-                       bound="latency", peak_ratio=1.0,
-                       text="Out = A @ B.T, A 128x64, B 64x64 f16, fp32 out, one CTA"),
-}
+def peaks_block(sm_count, sm_mhz):
+    """The denominators side by side: measured cuBLAS bf16 burst and sustained
+    peaks, the tcgen05 rate times SMs times the sampled and the maximum clock,
+    and the datasheet's dense figure."""
+    burst, sustained, kind = peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            max_mhz = float(json.load(f).get("sm_max_mhz") or 2070.0)
+    except Exception:
+        max_mhz = 2070.0
+    return {"bf16_burst_measured": burst if kind == "measured" else None,
+            "bf16_sustained_measured": sustained,
+            "bf16_computed_at_sampled_clock": computed_peak("bf16", sm_count, sm_mhz),
+            "bf16_computed_at_max_clock": computed_peak("bf16", sm_count, max_mhz),
+            "bf16_datasheet_dense": 2250.0, "unit": "TFLOP/s",
+            "computed_from": "%d SMs x %d flop/cycle/SM (kind::f16, measured) x SM clock" % (
+                sm_count, MMA_FLOP_PER_CYCLE_SM["bf16"])}
+
+
+def setup_workload(dg, torch, name):
+    """Inputs of a workload on the GPU, its plan and a one-launch step function."""
+    from dense_gemm_blackwell_gb300 import inputs
+    prob = inputs.make(name)
+    wl = prob.wl
+    code = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32, "e4m3": dg.GEMM_E4M3,
+            "e5m2": dg.GEMM_E5M2, "e2m1": dg.GEMM_E2M1}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    mode = wl.extra.get("scale_mode")
+    if mode == "mx":
+        smode = dg.GEMM_SCALE_MX_E8M0_32
+    elif mode == "nv":
+        smode = dg.GEMM_SCALE_NV_E4M3_16
+    else:
+        smode = dg.GEMM_SCALE_BLOCK_1x128_128x128 if wl.block_scaled else dg.GEMM_SCALE_NONE
+    t = {"A": prob.A.cuda(), "B": prob.B.cuda(),
+         "SA": prob.scale_a.cuda() if prob.scale_a is not None else None,
+         "SB": prob.scale_b.cuda() if prob.scale_b is not None else None,
+         "TS": torch.tensor(prob.tensor_scales, dtype=torch.float32, device="cuda") if mode == "nv" else None}
+    dshape = (wl.batch, wl.M, wl.N) if wl.batch > 1 else (wl.M, wl.N)
+    t["D"] = torch.empty(dshape, dtype=tdt[wl.dtype_out], device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=code[wl.dtype_in],
+                        dtype_b=code[wl.extra.get("dtype_b", wl.dtype_in)], dtype_d=code[wl.dtype_out],
+                        scale_mode=smode)
+    plan = dg.Plan(desc)
+    sptr = torch.cuda.current_stream().cuda_stream
+    ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    a, b, d, sa, sb, ts = (ptr(t[k]) for k in ("A", "B", "D", "SA", "SB", "TS"))
+    handle = plan.handle
+    if mode in ("mx", "nv"):
+        def step():
+            st = dg.gemm_run_mx(handle, a, b, d, sa, sb, ts, sptr)
+            if st != dg.GEMM_OK:
+                raise dg.GemmError(st, "gemm_run_mx")
+    else:
+        def step():
+            st = dg.gemm_run(handle, a, b, d, sa, sb, sptr)
+            if st != dg.GEMM_OK:
+                raise dg.GemmError(st, "gemm_run")
+    return {"prob": prob, "wl": wl, "t": t, "plan": plan, "info": plan.info.as_dict(), "step": step,
+            "flops": float(wl.flops), "bytes": working_set_bytes(name)}
+
+
+def computed_peak(rate: str, sm_count: int, mhz):
+    """SMs x tcgen05 flop per cycle per SM x SM clock (TFLOP/s), or None."""
+    if not mhz:
+        return None
+    return sm_count * MMA_FLOP_PER_CYCLE_SM[rate] * mhz * 1e6 / 1e12
+
+
+def roofline_for(name, mean_launch_ms, sm_count, sm_mhz):
+    winfo = WORKLOAD_INFO[name]
+    flops = 0.0
+    from dense_gemm_blackwell_gb300 import inputs
+    flops = float(inputs.WORKLOADS[name].flops)
+    nbytes = working_set_bytes(name)
+    peak_bf16, peak_bf16_sustained, peak_kind = peaks()
+    if winfo["bound"] == "hbm":
+        hbm, kind = hbm_peak()
+        achieved = nbytes / (mean_launch_ms / 1e3) / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+             "traffic": profiled_traffic(name), "peak_kind": kind}
+    elif winfo["bound"] == "latency":
+        r = {"bound": "latency", "achieved": mean_launch_ms * 1e3, "peak": None, "unit": "us/launch", "frac": None,
+             "traffic": profiled_traffic(name),
+             "note": "launch-latency bound (one CTA, 1 MFLOP): no throughput roofline applies"}
+    else:
+        peak = peak_bf16 * winfo["peak_ratio"]
+        achieved = flops / (mean_launch_ms / 1e3) / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+             "traffic": profiled_traffic(name),
+             "peak_kind": ("%s burst bf16 (MEASURED_PEAKS.json)%s" % (
+                 peak_kind, "" if winfo["peak_ratio"] == 1 else " x %g (nominal %s/bf16 dense ratio of GB300)" % (
+                     winfo["peak_ratio"], winfo["rate"]))) if peak_kind == "measured" else "fallback 1900 TFLOP/s bf16"}
+        if peak_bf16_sustained:
+            r["frac_of_sustained"] = achieved / (peak_bf16_sustained * winfo["peak_ratio"])
+        comp = computed_peak(winfo["rate"], sm_count, sm_mhz)
+        if comp:
+            r["computed_peak"] = comp
+            r["frac_of_computed"] = achieved / comp
+    r["algorithmic_flops_per_launch"] = flops
+    r["algorithmic_bytes_per_launch"] = nbytes
+    return r
+
+
+def metric_value(name, elapsed_ms, launches, world=1):
+    winfo = WORKLOAD_INFO[name]
+    from dense_gemm_blackwell_gb300 import inputs
+    if winfo["unit"] == "GB/s":
+        return working_set_bytes(name) * world * launches / (elapsed_ms / 1e3) / 1e9
+    if winfo["unit"] == "us/launch":
+        return elapsed_ms * 1e3 / launches
+    return inputs.WORKLOADS[name].flops * world * launches / (elapsed_ms / 1e3) / 1e12
+
+
+def measure_other(dg, torch, name, sampler, sm_count, target_ms=200.0):
+    """One other workload: warm-up, a timed region of back-to-back launches
+    (about target_ms long), clocks sampled inside it, its roofline."""
+    w = setup_workload(dg, torch, name)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        w["step"]()
+    torch.cuda.synchronize()
+    st, rec = w["plan"].sync_status()
+    if st != dg.GEMM_OK:
+        raise dg.GemmError(st, "%s warm-up device status" % name)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        w["step"]()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = int(min(50000, max(20, target_ms / max(e0.elapsed_time(e1) / 10, 1e-3))))
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(launches):
+        w["step"]()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    total_ms = e0.elapsed_time(e1)
+    st, rec = w["plan"].sync_status()
+    if st != dg.GEMM_OK:
+        raise dg.GemmError(st, "%s timed-region device status" % name)
+    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+    info = w["info"]
+    entry = {"metric": WORKLOAD_INFO[name]["metric"], "value": metric_value(name, total_ms, launches),
+             "unit": WORKLOAD_INFO[name]["unit"], "launches": launches, "ms_per_launch": total_ms / launches,
+             "dtype": w["wl"].dtype_in, "config": config_for(name),
+             "plan": {k: info[k] for k in ("kernel", "cta_group", "tile_m", "tile_n", "tile_k", "stages",
+                                            "tmem_stages", "grid", "num_tiles", "smem_bytes")},
+             "roofline": roofline_for(name, total_ms / launches, sm_count, clocks.get("sm_mhz")),
+             "clocks": clocks}
+    w["plan"].close()
+    del w
+    torch.cuda.empty_cache()
+    return entry
 
 
 def run_ours(args):
@@ -289,32 +520,19 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
     winfo = WORKLOAD_INFO[args.workload]
-    prob = inputs.make(args.workload)
-    wl = prob.wl
     dg.build()
-    code = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32, "e4m3": dg.GEMM_E4M3}
+    w = setup_workload(dg, torch, args.workload)
+    prob, wl, plan, info, step = w["prob"], w["wl"], w["plan"], w["info"], w["step"]
+    A, B, D, SA, SB = (w["t"][k] for k in ("A", "B", "D", "SA", "SB"))
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    A = prob.A.cuda()
-    B = prob.B.cuda()
-    SA = prob.scale_a.cuda() if prob.scale_a is not None else None
-    SB = prob.scale_b.cuda() if prob.scale_b is not None else None
-    dshape = (wl.batch, wl.M, wl.N) if wl.batch > 1 else (wl.M, wl.N)
-    D = torch.empty(dshape, dtype=tdt[wl.dtype_out], device="cuda")
-    desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=code[wl.dtype_in], dtype_d=code[wl.dtype_out],
-                        scale_mode=dg.GEMM_SCALE_BLOCK_1x128_128x128 if wl.block_scaled else dg.GEMM_SCALE_NONE)
-    plan = dg.Plan(desc)
-    info = plan.info.as_dict()
+    dshape = tuple(D.shape)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
-    flops = float(wl.flops)
+    flops = w["flops"]
     nbytes = lambda t: 0 if t is None else t.numel() * t.element_size()  # noqa: E731
-    alg_bytes = float(nbytes(A) + nbytes(B) + nbytes(D) + nbytes(SA) + nbytes(SB))
+    alg_bytes = w["bytes"]
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
-
-    def step():
-        s = dg.gemm_run(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), ptr(SA), ptr(SB), sptr)
-        if s != dg.GEMM_OK:
-            raise dg.GemmError(s, "gemm_run")
+    sm_count = torch.cuda.get_device_properties(0).multi_processor_count
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -364,39 +582,10 @@ def run_ours(args):
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
 
-    def metric_value(elapsed_ms, steps):
-        if winfo["unit"] == "GB/s":
-            return alg_bytes * world * steps / (elapsed_ms / 1e3) / 1e9
-        if winfo["unit"] == "us/launch":
-            return elapsed_ms * 1e3 / steps
-        return flops * world * steps / (elapsed_ms / 1e3) / 1e12
-
-    value = metric_value(total_ms, args.steps)
-
+    value = metric_value(args.workload, total_ms, args.steps, world)
     # roofline of the dominant (only) kernel, from its own launch events
-    peak_bf16, peak_bf16_sustained, peak_kind = peaks()
     mean_launch_ms = total_ms / args.steps
-    if winfo["bound"] == "hbm":
-        hbm, kind = hbm_peak()
-        achieved = alg_bytes / (mean_launch_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": None, "peak_kind": kind}
-    else:
-        peak = peak_bf16 * winfo["peak_ratio"]
-        achieved = flops / (mean_launch_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak,
-                    "traffic": profiled_traffic() if args.workload == WORKLOAD else None,
-                    "peak_kind": ("%s burst bf16 (MEASURED_PEAKS.json)%s" %
-                                  (peak_kind, " x 2 (fp8/bf16 nominal ratio 4.5/2.25)" if winfo["peak_ratio"] != 1 else ""))
-                    if peak_kind == "measured" else "fallback 1900 TFLOP/s bf16"}
-        if peak_bf16_sustained:
-            roofline["frac_of_sustained"] = achieved / (peak_bf16_sustained * winfo["peak_ratio"])
-        if winfo["bound"] == "latency":
-            roofline["bound"] = "tensor"
-            roofline["note"] = "launch-latency bound: 1 CTA; value is microseconds per launch"
-    roofline["algorithmic_flops_per_launch"] = flops
-    roofline["algorithmic_bytes_per_launch"] = alg_bytes
+    roofline = roofline_for(args.workload, mean_launch_ms, sm_count, clocks.get("sm_mhz"))
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     hA = prob.A.pin_memory()
@@ -409,11 +598,24 @@ def run_ours(args):
     # and a longer run keeps one such step from dominating the average
     e2e_steps = max(3, min(args.steps, 100))
 
-    def e2e_step():
-        s = dg.gemm_run_host(plan.handle, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), ptr(hSA), ptr(hSB),
-                             A.data_ptr(), B.data_ptr(), D.data_ptr(), ptr(SA), ptr(SB), sptr)
-        if s != dg.GEMM_OK:
-            raise dg.GemmError(s, "gemm_run_host")
+    if wl.extra.get("scale_mode") in ("mx", "nv"):
+        # gemm_run_host does not take tiled scales: copy in, gemm_run_mx, copy out
+        dTS = w["t"]["TS"]
+
+        def e2e_step():
+            for dev, host in ((A, hA), (B, hB), (SA, hSA), (SB, hSB)):
+                dev.copy_(host, non_blocking=True)
+            s = dg.gemm_run_mx(plan.handle, A.data_ptr(), B.data_ptr(), D.data_ptr(), SA.data_ptr(), SB.data_ptr(),
+                               ptr(dTS), sptr)
+            if s != dg.GEMM_OK:
+                raise dg.GemmError(s, "gemm_run_mx")
+            hD.copy_(D, non_blocking=True)
+    else:
+        def e2e_step():
+            s = dg.gemm_run_host(plan.handle, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), ptr(hSA), ptr(hSB),
+                                 A.data_ptr(), B.data_ptr(), D.data_ptr(), ptr(SA), ptr(SB), sptr)
+            if s != dg.GEMM_OK:
+                raise dg.GemmError(s, "gemm_run_host")
 
     # warm-up: the first calls create the host pipeline's streams, events and
     # panel plans and encode their tensor maps
@@ -435,7 +637,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1)
     e2e_step_ms = [e2e_marks[i].elapsed_time(e2e_marks[i + 1]) for i in range(e2e_steps)]
     e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
-    e2e_value = metric_value(e2e_ms, e2e_steps)
+    e2e_value = metric_value(args.workload, e2e_ms, e2e_steps, world)
     st, rec = plan.sync_status()
     if st != dg.GEMM_OK:
         raise dg.GemmError(st, "e2e device status")
@@ -451,15 +653,11 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
         "higher_is_better": winfo["unit"] != "us/launch", "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype_in, "data": "synthetic",
-        "config": {"workload": "%s: %s" % (args.workload, winfo["text"]),
-                   "M": wl.M, "N": wl.N, "K": wl.K, "batch": wl.batch,
-                   "inputs": "%s seed %d" % (wl.dist, wl.seed),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": ("no flush: working set %.0f MB > 129 MB L2" % (alg_bytes / 1e6)) if alg_bytes > 129e6
-                   else "no flush: working set %.1f MB fits L2 (L2-warm)" % (alg_bytes / 1e6),
-                   "plan": {k: info[k] for k in ("kernel", "cta_group", "tile_m", "tile_n", "tile_k", "stages",
-                                                  "tmem_stages", "grid", "num_tiles", "smem_bytes")}},
+        "config": config_for(args.workload, world),
+        "plan": {k: info[k] for k in ("kernel", "cta_group", "tile_m", "tile_n", "tile_k", "stages",
+                                       "tmem_stages", "grid", "num_tiles", "smem_bytes")},
         "roofline": roofline,
+        "peaks": peaks_block(sm_count, clocks.get("sm_mhz")),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": winfo["unit"], "steps": e2e_steps,
                 "h2d_bytes_per_step": int(nbytes(hA) + nbytes(hB) + nbytes(hSA) + nbytes(hSB)),
@@ -472,6 +670,19 @@ def run_ours(args):
                       "separate_pass": {"launches": len(launch_ms), "min": min(launch_ms), "max": max(launch_ms),
                                         "median": statistics.median(launch_ms)}},
     }
+    if rank == 0 and world == 1 and args.workload == WORKLOAD and not args.no_other_workloads:
+        # the rest of the suite, each with its own timed region, clocks and roofline
+        plan.close()
+        del w, A, B, D, SA, SB, hA, hB, hD, hSA, hSB
+        torch.cuda.empty_cache()
+        sampler = ClockSampler(local_rank)
+        sampler.start()
+        time.sleep(0.3)
+        others = {}
+        for name, _ in OTHER_WORKLOADS:
+            others[name] = measure_other(dg, torch, name, sampler, sm_count)
+        sampler.stop()
+        line["other_workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
@@ -489,6 +700,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOAD_INFO), default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only --workload (profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

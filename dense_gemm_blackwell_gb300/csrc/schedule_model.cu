@@ -103,9 +103,13 @@ gemm_status_t gemm_schedule_choose(const gemm_sched_params_t* in, int32_t max_st
 //    copy of the persistent kernel with its MMAs skipped streamed 8192^3's
 //    operands at 657 cycles per 32 KB stage and 912 per 64 KB stage;
 //  * tcgen05.ld 220 bytes per cycle per SM while the MMAs run (200-240 measured);
-//  * load latency 900 and hand-back 600 cycles: estimates (the model's runs at
-//    three or more stages and two accumulators do not depend on them).
-constexpr gemm_machine_t kGb300 = {8192.0, 400.0, 128.0, 900.0, 220.0, 600.0};
+//  * load latency 1,400 cycles: the value whose model best matches a sweep of
+//    the ring depth at 8192^3 (512-wide tiles: 2 stages 39 % slower than 4,
+//    3 stages 1.6 % slower; 256-wide tiles of 128-deep stages: 2 stages 21 %
+//    slower than 3);
+//  * hand-back 600 cycles: an estimate (runs with two accumulators do not
+//    depend on it).
+constexpr gemm_machine_t kGb300 = {8192.0, 400.0, 128.0, 1400.0, 220.0, 600.0};
 
 gemm_status_t gemm_machine_gb300(gemm_machine_t* out) {
     if (!out) return GEMM_ERR_INVALID_ARG;

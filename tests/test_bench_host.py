@@ -56,13 +56,43 @@ def test_clock_summary():
 
 
 def test_traffic_is_reported_only_for_the_profiled_sources(tmp_path, monkeypatch):
-    """The committed summary's DRAM bytes count only while its recorded source
-    hash matches the current kernel sources."""
-    text = open(bench.PROFILE).read()
+    """A committed summary's DRAM bytes count only while its recorded source
+    hash matches the current sources of that workload's kernel."""
+    name = bench.WORKLOAD
     fake = tmp_path / "profile.md"
-    fake.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 1.5e9\n" % bench.kernel_source_hash())
-    monkeypatch.setattr(bench, "PROFILE", str(fake))
-    assert bench.profiled_traffic() == 1.5e9
+    fake.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 1.5e9\n" % bench.kernel_source_hash(name))
+    info = dict(bench.WORKLOAD_INFO[name], profile=str(fake))
+    monkeypatch.setitem(bench.WORKLOAD_INFO, name, info)
+    assert bench.profiled_traffic(name) == 1.5e9
     fake.write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 1.5e9\n")
-    assert bench.profiled_traffic() is None
-    assert "kernel_source_sha256_16" in text and "dram_bytes_per_launch" in text
+    assert bench.profiled_traffic(name) is None
+    # each kernel family hashes its own sources
+    assert bench.kernel_source_hash("mxfp8_8192") != bench.kernel_source_hash("fp8_block8192")
+    assert bench.kernel_source_hash("square4096_bf16") == bench.kernel_source_hash(name)
+
+
+def test_every_workload_has_a_profile_path_and_known_kernel():
+    for name, info in bench.WORKLOAD_INFO.items():
+        assert info["kernel"] in bench.SOURCES and info["profile"].startswith(os.path.join(ROOT, "profiles"))
+        assert info["rate"] in bench.MMA_FLOP_PER_CYCLE_SM
+    assert {n for n, _ in bench.OTHER_WORKLOADS} | {bench.WORKLOAD} == set(bench.WORKLOAD_INFO)
+
+
+def test_algorithmic_bytes():
+    MB = 1 << 20
+    assert bench.working_set_bytes("square8192_bf16") == 512 * MB            # A, B bf16 + D fp32
+    assert bench.working_set_bytes("batched256_f16") == 512 * 3 * 256 * 256 * 2
+    # e4m3 A, B + bf16 D + fp32 scales [8192][64] and [64][64]
+    assert bench.working_set_bytes("fp8_block8192") == 64 * MB * 2 + 128 * MB + 4 * (8192 * 64 + 64 * 64)
+    # MXFP8: + 512-byte scale tiles, 64 row blocks x 64 K groups per operand
+    assert bench.working_set_bytes("mxfp8_8192") == 64 * MB * 2 + 128 * MB + 2 * 512 * 64 * 64
+    # NVFP4: 4-bit operands, E4M3 scales per 16 (128 K groups), two fp32 tensor scales
+    assert bench.working_set_bytes("nvfp4_8192") == 32 * MB * 2 + 128 * MB + 2 * 512 * 64 * 128 + 8
+
+
+def test_both_arms_share_the_config():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "single_cta", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    j = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
+    assert j["config"] == bench.config_for("single_cta", 1)

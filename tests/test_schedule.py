@@ -151,3 +151,28 @@ def test_plan_schedule_rejects_what_it_does_not_model():
     desc = dg.make_desc(4096, 4096, 4096, dtype_a=dg.GEMM_BF16)
     st, info = dg.gemm_plan_query(desc, props)
     assert dg.gemm_plan_schedule(desc, info, props, bad)[0] == dg.GEMM_ERR_INVALID_ARG
+
+
+# Ring-depth sweep of the 8192^3 bf16 -> bf16 plans on GB300 (medians of
+# 10-launch groups, CUDA events): time relative to the planner's depth.
+STAGE_SWEEP_512 = {4: 1.000, 3: 1.016, 2: 1.388}
+STAGE_SWEEP_256_K128 = {3: 1.000, 2: 1.212}
+
+
+def _run(over, stages):
+    props = dg.GemmDeviceProps(**GB300)
+    desc = dg.make_desc(8192, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, stages=stages, **over)
+    st, info = dg.gemm_plan_query(desc, props)
+    assert st == dg.GEMM_OK
+    return dg.gemm_plan_schedule(desc, info, props)[2].run_length
+
+
+def test_model_reproduces_the_ring_depth_sweep():
+    """512-wide tiles: three stages are as good as four (measured +1.6 %), two
+    are far slower (measured +39 %); the model agrees on both, within 5 points."""
+    base = _run({}, 4)
+    for s, measured in STAGE_SWEEP_512.items():
+        assert abs(_run({}, s) / base - measured) < 0.05, (s, _run({}, s) / base, measured)
+    # 256-wide tiles with 128-deep stages: two stages are too few in both
+    over = dict(tile_n=256, flags=dg.GEMM_FLAG_CTA_GROUP_2)
+    assert _run(over, 2) / _run(over, 3) > 1 + (STAGE_SWEEP_256_K128[2] - 1) / 2
