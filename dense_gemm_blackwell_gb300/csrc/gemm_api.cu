@@ -631,6 +631,13 @@ gemm_status_t noalloc_address(int dev, void** out) {
     return GEMM_OK;
 }
 
+// Drop the cached address of device `dev` (looked up again on the next call).
+void noalloc_forget(int dev) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    g_noalloc_addr[dev] = nullptr;
+}
+
 }  // namespace
 
 constexpr int kHostPanels = 8;    // gemm_run_host: at most this many row (or batch) panels
@@ -1333,8 +1340,12 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
     p.status = static_cast<gemm_device_error_t*>(record);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     noalloc_clear_kernel<<<1, 32, 0, stream>>>((unsigned)sizeof(gemm_device_error_t));
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaGetLastError()) != cudaSuccess) {
+        noalloc_forget(dev);
+        return cuda_fail(e);
+    }
     s = gemm_run(&p, A, B, D, scale_a, scale_b, stream_);
+    if (s == GEMM_ERR_CUDA) noalloc_forget(dev);      // e.g. a context reset moved the array
     if (s != GEMM_OK || status_out == nullptr) return s;
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemcpy(status_out, record, sizeof(*status_out), cudaMemcpyDeviceToHost)) != cudaSuccess)

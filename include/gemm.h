@@ -336,6 +336,9 @@ gemm_status_t gemm_sync_status(gemm_plan_t plan, gemm_stream_t stream, gemm_devi
  * process exits; no problem size needs more, and a build whose record did not
  * fit would return GEMM_ERR_RESOURCES.  The first call on each device looks up
  * the array's device address; make that first call before any stream capture.
+ * A reset of the device's primary context (cudaDeviceReset) reloads the
+ * library's device code and moves the array: a call that then fails with
+ * GEMM_ERR_CUDA drops the cached address, and the next call looks it up again.
  * Each call clears the record on `stream`, then enqueues the product; the
  * record keeps the last call's contents.  All calls share this one record, so
  * calls whose work overlaps on the GPU (other streams, other host threads)
