@@ -86,3 +86,34 @@ def test_fp8_dropped_copy_times_out_and_context_survives(cg_flag):
     dref, sabs = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="e4m3", dtype_b="e4m3",
                              scale_a=prob.scale_a.numpy(), scale_b=prob.scale_b.numpy())
     assert compare(D.double().cpu().numpy(), dref[0], sabs[0], "bf16", TOL_FP8)["ok"]
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+def test_mx_dropped_copy_times_out_and_context_survives(cg_flag):
+    """Same for the hardware block-scaled kernel, whose full barriers also
+    count the scale producer's bytes."""
+    prob = inputs.make("mxfp8_8192", M=1024, N=1024, K=1024, dist="ints", seed=44)
+    wl = prob.wl
+    A, B = prob.A.cuda(), prob.B.cuda()
+    SA, SB = prob.scale_a.cuda(), prob.scale_b.cuda()
+    D = torch.zeros(wl.M, wl.N, device="cuda")
+    common = dict(dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_F32, scale_mode=dg.GEMM_SCALE_MX_E8M0_32)
+    desc = dg.make_desc(wl.M, wl.N, wl.K, flags=cg_flag | dg.GEMM_FLAG_TEST_DROP_LOAD,
+                        wait_timeout_ns=20_000_000, **common)
+    with dg.Plan(desc) as plan:
+        t0 = time.time()
+        plan.run_mx(A, B, D, SA, SB)
+        status, rec = plan.sync_status()
+        elapsed = time.time() - t0
+        assert status == dg.GEMM_ERR_TIMEOUT
+        assert rec.code == dg.GEMM_ERR_TIMEOUT and rec.role in (1, 2, 3)
+        assert elapsed < 5.0
+        assert plan.sync_status()[0] == dg.GEMM_OK
+
+    desc_ok = dg.make_desc(wl.M, wl.N, wl.K, flags=cg_flag, **common)
+    with dg.Plan(desc_ok) as plan:
+        plan.run_mx(A, B, D, SA, SB)
+        assert plan.sync_status()[0] == dg.GEMM_OK
+    dref, _ = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, dtype_a="e4m3", dtype_b="e4m3",
+                          scale_a=prob.scale_a, scale_b=prob.scale_b, scale_mode="mx")
+    assert np.array_equal(D.double().cpu().numpy(), dref[0])

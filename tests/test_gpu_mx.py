@@ -153,3 +153,45 @@ def test_wrong_entry_points_are_refused():
                               sb.data_ptr(), None, stream) == dg.GEMM_ERR_ALIGNMENT
     assert dg.gemm_run_noalloc(desc, A.data_ptr(), B.data_ptr(), D.data_ptr(), None, None, stream,
                                None) == dg.GEMM_ERR_UNSUPPORTED
+
+
+def _batched(name, batch, seed0, **shape):
+    """A batch of independent problems with the workload's recipe: operands
+    stacked, tiled scales one batch entry after the other."""
+    probs = [inputs.make(name, dist="ints", seed=seed0 + i, **shape) for i in range(batch)]
+    return (probs, torch.stack([p.A for p in probs]), torch.stack([p.B for p in probs]),
+            torch.cat([p.scale_a for p in probs]), torch.cat([p.scale_b for p in probs]))
+
+
+@pytest.mark.parametrize("name,cg_flag", [("mxfp8_8192", dg.GEMM_FLAG_CTA_GROUP_2),
+                                          ("mxfp4_8192", dg.GEMM_FLAG_CTA_GROUP_1),
+                                          ("nvfp4_8192", dg.GEMM_FLAG_CTA_GROUP_2)])
+def test_batched_block_scaled_bit_exact(name, cg_flag):
+    """Three batch entries: 3-D operand maps and the scale maps' batch dimension."""
+    shape = dict(M=300, N=260, K=256)
+    probs, A, B, SA, SB = _batched(name, 3, 61, **shape)
+    wl = probs[0].wl
+    mode = wl.extra["scale_mode"]
+    D = torch.full((3, wl.M, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, batch=3, dtype_a=IN[wl.dtype_in], dtype_d=dg.GEMM_F32,
+                        scale_mode=MODE[mode], flags=cg_flag)
+    ts = torch.tensor(probs[0].tensor_scales, dtype=torch.float32, device="cuda") if mode == "nv" else None
+    with dg.Plan(desc) as plan:
+        plan.run_mx(A.cuda(), B.cuda(), D, SA.cuda(), SB.cuda(), ts)
+        assert plan.sync_status()[0] == dg.GEMM_OK
+    dref, _ = oracle.gemm(A, B, M=wl.M, N=wl.N, K=wl.K, batch=3, dtype_a=wl.dtype_in, dtype_b=wl.dtype_in,
+                          scale_a=SA, scale_b=SB, scale_mode=mode, tensor_scales=probs[0].tensor_scales)
+    assert np.array_equal(D.double().cpu().numpy(), dref)
+
+
+def test_empty_and_k_zero():
+    """K = 0 writes zeros (no scale pointers are read); M = 0 is a no-op."""
+    for M, N, K in [(300, 64, 0), (0, 64, 64)]:
+        D = torch.full((max(M, 1), N), 7.0, device="cuda")
+        desc = dg.make_desc(M, N, K, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_F32, scale_mode=dg.GEMM_SCALE_MX_E8M0_32,
+                            lda=64, ldb=64, ldd=N)
+        dummy = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+        with dg.Plan(desc) as plan:
+            plan.run_mx(dummy, dummy, D, dummy, dummy)
+            torch.cuda.synchronize()
+        assert (D == 0).all() if (K == 0 and M) else (D == 7.0).all()
