@@ -76,7 +76,6 @@ __device__ void mx_scale_producer(const MxParams& q, uint8_t* sf_ring, uint32_t 
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
-    int issued = 0;
     WorkUnit u;
     for (int idx = 0; !aborted && next_unit(p, cluster_id, num_clusters, idx, u); ++idx) {
         int b, mb, nb;
@@ -105,10 +104,11 @@ __device__ void mx_scale_producer(const MxParams& q, uint8_t* sf_ring, uint32_t 
                 }
             }
             __syncwarp();
-            ++issued;
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
     }
+    // On abort the copies this warp issued land on the stages' full barriers,
+    // whose phases the A producer drains (bounded) before the CTA exits.
     if (!aborted) {
         // tail: every slot released, so no commit lands on an exited CTA
         for (int i = 0; i < S; ++i) {
@@ -118,7 +118,6 @@ __device__ void mx_scale_producer(const MxParams& q, uint8_t* sf_ring, uint32_t 
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
     }
-    (void)issued;
 }
 
 // MMA issuer (the pair leader's warp 1; one elected lane issues).
