@@ -195,3 +195,24 @@ def test_empty_and_k_zero():
             plan.run_mx(dummy, dummy, D, dummy, dummy)
             torch.cuda.synchronize()
         assert (D == 0).all() if (K == 0 and M) else (D == 7.0).all()
+
+
+def _random_cases(n=12, seed=2027):
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        name = rng.choice(["mxfp8_8192", "mxfp4_8192", "nvfp4_8192"])
+        kq = 16 if name == "mxfp8_8192" else 32            # rows of K must be 16-byte multiples
+        cases.append(dict(name=name, M=rng.randint(1, 700), N=8 * rng.randint(1, 90), K=kq * rng.randint(1, 40),
+                          cg=rng.choice([dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2]),
+                          out=rng.choice(["f32", "bf16", "f16"]), ctas=rng.choice([0, 4, 10]), seed=100 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "%s-%dx%dx%d" % (c["name"], c["M"], c["N"], c["K"]))
+def test_random_shapes_bit_exact(case):
+    """Seeded random shapes: any M, N a multiple of 8, K a multiple of 16 (8-bit) or
+    32 (4-bit), either CTA group, every output type, capped grids."""
+    prob = inputs.make(case["name"], dist="ints", seed=case["seed"], M=case["M"], N=case["N"], K=case["K"])
+    check(prob, case["out"], exact=True, flags=case["cg"], max_ctas=case["ctas"])
