@@ -99,13 +99,19 @@ WORKLOAD_INFO = {
                        profile=_prof("mx_pair_nvfp4_8192_bf16.md"),
                        text="D = tA tB (qA . sA)(qB . sB)^T, 8192^3, e2m1 TN (packed), E4M3 scale per 16 K elements "
                             "(tcgen05 block scaling), bf16 out"),
+    "square8192_bf16_tile256": dict(
+        metric="GEMM TFLOP/s (bf16 in, fp32 acc, 8192^3, cta_group::2 256x256 tiles)", unit=UNIT, bound="tensor",
+        peak_ratio=1.0, rate="bf16", kernel="persistent", data="square8192_bf16",
+        desc=dict(tile_n=256, flags=2),        # GEMM_FLAG_CTA_GROUP_2: the pair form with 256-wide tiles
+        profile=_prof("persistent_pair_square8192_bf16_f32_tile256.md"),
+        text="D = A*B^T, M=N=K=8192, bf16 TN, fp32 accumulate, fp32 out, persistent grid, cta_group::2 256x256 tiles"),
     "single_cta": dict(metric="single-CTA GEMM latency (128x64x64 f16 -> f32)", unit="us/launch",
                        bound="latency", peak_ratio=1.0, rate="bf16", kernel="single",
                        profile=_prof("single_cta_128x64x64_f16.md"),
                        text="Out = A @ B.T, A 128x64, B 64x64 f16, fp32 out, one CTA"),
 }
 # the other workloads timed after the headline, with launches per timed region
-OTHER_WORKLOADS = [("single_cta", 2000), ("square4096_bf16", 400), ("batched256_f16", 600),
+OTHER_WORKLOADS = [("square8192_bf16_tile256", 200), ("single_cta", 2000), ("square4096_bf16", 400), ("batched256_f16", 600),
                    ("fp8_block8192", 100), ("mxfp8_8192", 100), ("mxfp4_8192", 200), ("nvfp4_8192", 200)]
 
 
@@ -131,10 +137,15 @@ def profiled_traffic(name: str = WORKLOAD):
     return float(m_tr.group(1))
 
 
+def data_of(name: str) -> str:
+    """The input workload (shapes, types, values) a bench entry runs on."""
+    return WORKLOAD_INFO[name].get("data", name)
+
+
 def config_for(name: str, world: int = 1) -> dict:
     """The `config` object of a workload's line (identical in both arms)."""
     from dense_gemm_blackwell_gb300 import inputs
-    wl = inputs.WORKLOADS[name]
+    wl = inputs.WORKLOADS[data_of(name)]
     winfo = WORKLOAD_INFO[name]
     ws = working_set_bytes(name)
     return {"workload": "%s: %s" % (name, winfo["text"]), "M": wl.M, "N": wl.N, "K": wl.K, "batch": wl.batch,
@@ -147,7 +158,7 @@ def config_for(name: str, world: int = 1) -> dict:
 def working_set_bytes(name: str) -> float:
     """Algorithmic bytes of one launch: A, B, D and any scales, once each."""
     from dense_gemm_blackwell_gb300 import inputs
-    wl = inputs.WORKLOADS[name]
+    wl = inputs.WORKLOADS[data_of(name)]
     bits = {"f16": 16, "bf16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}
     total = (wl.M + wl.N) * wl.K * wl.batch * bits[wl.dtype_in] / 8 + wl.M * wl.N * wl.batch * bits[wl.dtype_out] / 8
     mode = wl.extra.get("scale_mode")
@@ -306,7 +317,7 @@ def run_reference(args):
     import oracle
     from dense_gemm_blackwell_gb300 import inputs
     winfo = WORKLOAD_INFO[args.workload]
-    prob = inputs.make(args.workload)
+    prob = inputs.make(data_of(args.workload))
     wl = prob.wl
     t = time.perf_counter()
     _oracle_rows(prob, [0, 1])
@@ -371,7 +382,7 @@ def peaks_block(sm_count, sm_mhz):
 def setup_workload(dg, torch, name):
     """Inputs of a workload on the GPU, its plan and a one-launch step function."""
     from dense_gemm_blackwell_gb300 import inputs
-    prob = inputs.make(name)
+    prob = inputs.make(data_of(name))
     wl = prob.wl
     code = {"f16": dg.GEMM_F16, "bf16": dg.GEMM_BF16, "f32": dg.GEMM_F32, "e4m3": dg.GEMM_E4M3,
             "e5m2": dg.GEMM_E5M2, "e2m1": dg.GEMM_E2M1}
@@ -391,7 +402,7 @@ def setup_workload(dg, torch, name):
     t["D"] = torch.empty(dshape, dtype=tdt[wl.dtype_out], device="cuda")
     desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=code[wl.dtype_in],
                         dtype_b=code[wl.extra.get("dtype_b", wl.dtype_in)], dtype_d=code[wl.dtype_out],
-                        scale_mode=smode)
+                        scale_mode=smode, **WORKLOAD_INFO[name].get("desc", {}))
     plan = dg.Plan(desc)
     sptr = torch.cuda.current_stream().cuda_stream
     ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
@@ -420,9 +431,8 @@ def computed_peak(rate: str, sm_count: int, mhz):
 
 def roofline_for(name, mean_launch_ms, sm_count, sm_mhz):
     winfo = WORKLOAD_INFO[name]
-    flops = 0.0
     from dense_gemm_blackwell_gb300 import inputs
-    flops = float(inputs.WORKLOADS[name].flops)
+    flops = float(inputs.WORKLOADS[data_of(name)].flops)
     nbytes = working_set_bytes(name)
     peak_bf16, peak_bf16_sustained, peak_kind = peaks()
     if winfo["bound"] == "hbm":
@@ -460,7 +470,7 @@ def metric_value(name, elapsed_ms, launches, world=1):
         return working_set_bytes(name) * world * launches / (elapsed_ms / 1e3) / 1e9
     if winfo["unit"] == "us/launch":
         return elapsed_ms * 1e3 / launches
-    return inputs.WORKLOADS[name].flops * world * launches / (elapsed_ms / 1e3) / 1e12
+    return inputs.WORKLOADS[data_of(name)].flops * world * launches / (elapsed_ms / 1e3) / 1e12
 
 
 def measure_other(dg, torch, name, sampler, sm_count, target_ms=200.0):

@@ -265,10 +265,10 @@ def test_full_batched256_f16():
 # rounding to D's type must equal the oracle's rounding bit for bit.  A dropped,
 # repeated or misplaced K slice changes some element by an integer and fails.
 
-def check_sampled_exact(name, out_dtype, whole=False, expect=None):
+def check_sampled_exact(name, out_dtype, whole=False, expect=None, **desc_kw):
     prob = inputs.make(name, dist="ints")
     wl = prob.wl
-    D, info = run_gpu(prob, out_dtype)
+    D, info = run_gpu(prob, out_dtype, **desc_kw)
     if expect:
         assert {k: info[k] for k in expect} == expect, info
     if whole:
@@ -291,6 +291,14 @@ def check_sampled_exact(name, out_dtype, whole=False, expect=None):
 def test_full_square8192_bf16_f32_integers_bit_exact():
     check_sampled_exact("square8192_bf16", "f32",
                         expect={"cta_group": 2, "tile_n": 512, "tmem_stages": 1, "grid": 152, "stream_k_tiles": 0})
+
+
+@pytest.mark.slow
+def test_full_square8192_bf16_f32_256x256_pair_tiles_integers_bit_exact():
+    """The configuration's literal plan: cta_group::2 with 256 x 256 tiles (two
+    accumulators, two-atom stages, stream-K over the partial last wave)."""
+    check_sampled_exact("square8192_bf16", "f32", tile_n=256, flags=dg.GEMM_FLAG_CTA_GROUP_2,
+                        expect={"cta_group": 2, "tile_n": 256, "tmem_stages": 2})
 
 
 @pytest.mark.slow
