@@ -267,7 +267,9 @@ int mx_chunks(const gemm_desc_t& d) {
 }
 
 gemm_status_t plan_mx(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
-    if (d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) return GEMM_ERR_UNSUPPORTED;
+    // MN-major operands: 8-bit elements only (packed E2M1 is K-major), loaded as
+    // boxes of 128 contiguous M/N elements x 128 k-rows
+    if ((d.major_a != GEMM_K_MAJOR || d.major_b != GEMM_K_MAJOR) && !is8(d.dtype_a)) return GEMM_ERR_UNSUPPORTED;
     if (d.tile_n != 0 && d.tile_n != kMxTileN) return GEMM_ERR_UNSUPPORTED;
     if (d.flags & (GEMM_FLAG_SINGLE_CTA | GEMM_FLAG_ACCUM_F16 | GEMM_FLAG_STAGE_K2 | GEMM_FLAG_EPILOGUE_DIRECT))
         return GEMM_ERR_UNSUPPORTED;
@@ -968,6 +970,7 @@ gemm_status_t gemm_run_mx(gemm_plan_t plan, const void* A, const void* B, void* 
     const bool fp4 = is4(d.dtype_a);
     if (fp4 && ((d.lda | d.ldb | d.stride_a | d.stride_b) & 1)) return GEMM_ERR_INVALID_ARG;
     const int64_t kbytes = fp4 ? d.K / 2 : d.K;
+    const bool mn_a = d.major_a == GEMM_MN_MAJOR, mn_b = d.major_b == GEMM_MN_MAJOR;
     const int64_t lda_b = fp4 ? d.lda / 2 : d.lda, ldb_b = fp4 ? d.ldb / 2 : d.ldb;
     const int64_t sta_b = fp4 ? d.stride_a / 2 : d.stride_a, stb_b = fp4 ? d.stride_b / 2 : d.stride_b;
     if ((lda_b & 15) || (ldb_b & 15)) return GEMM_ERR_ALIGNMENT;
@@ -979,9 +982,14 @@ gemm_status_t gemm_run_mx(gemm_plan_t plan, const void* A, const void* B, void* 
     const int64_t kq = std::max<int64_t>(ceil_div(ceil_div(d.K, v), 4), 1);
     if (!plan->maps_valid || plan->map_ptrs[0] != A || plan->map_ptrs[1] != B || plan->map_ptrs[2] != D) {
         plan->maps_valid = false;
-        // byte boxes of one 128-byte K atom x 128 rows (A) or 256 / cg rows (B)
-        if (!encode_map(&plan->maps[0], GEMM_E4M3, A, kbytes, d.M, lda_b, d.batch, sta_b, 128, 128) ||
-            !encode_map(&plan->maps[1], GEMM_E4M3, B, kbytes, d.N, ldb_b, d.batch, stb_b, 128, kMxTileN / cg) ||
+        // byte boxes of one 128-byte K atom x 128 rows (A) or 256 / cg rows (B);
+        // MN-major: 128 contiguous M (N) bytes x 128 k-rows
+        const bool ok_a = mn_a ? encode_map(&plan->maps[0], GEMM_E4M3, A, d.M, d.K, lda_b, d.batch, sta_b, 128, 128)
+                               : encode_map(&plan->maps[0], GEMM_E4M3, A, kbytes, d.M, lda_b, d.batch, sta_b, 128, 128);
+        const bool ok_b = mn_b ? encode_map(&plan->maps[1], GEMM_E4M3, B, d.N, d.K, ldb_b, d.batch, stb_b, 128, 128)
+                               : encode_map(&plan->maps[1], GEMM_E4M3, B, kbytes, d.N, ldb_b, d.batch, stb_b, 128,
+                                            kMxTileN / cg);
+        if (!ok_a || !ok_b ||
             !encode_map(&plan->maps[2], d.dtype_d, D, d.N, d.M, d.ldd, d.batch, d.stride_d, 128 / eb_d, 32)) {
             g_last_cuda_error = (int)cudaErrorInvalidValue;
             return GEMM_ERR_CUDA;
@@ -1019,10 +1027,13 @@ gemm_status_t gemm_run_mx(gemm_plan_t plan, const void* A, const void* B, void* 
     p.tile_k = 128;                         // the producers' K coordinate counts bytes
     p.k_atoms = 1;
     p.mn_box_elems = 128;
+    p.mn_major_a = mn_a ? 1 : 0;
+    p.mn_major_b = mn_b ? 1 : 0;
     // element formats: mxf8f6f4 0 = E4M3, 1 = E5M2; mxf4 / mxf4nvf4 1 = E2M1; scales UE8M0 (MX) or UE4M3 (NV)
     const uint32_t fa = fp4 ? 1u : (d.dtype_a == GEMM_E5M2 ? 1u : 0u);
     const uint32_t fb = fp4 ? 1u : (d.dtype_b == GEMM_E5M2 ? 1u : 0u);
-    p.idesc = dgb::make_idesc_block_scaled(fa, fb, (uint32_t)info.tile_m, (uint32_t)info.tile_n, nv ? 0u : 1u);
+    p.idesc = dgb::make_idesc_block_scaled(fa, fb, (uint32_t)info.tile_m, (uint32_t)info.tile_n, nv ? 0u : 1u,
+                                           (uint32_t)p.mn_major_a, (uint32_t)p.mn_major_b);
     p.stage_bytes_a = 128u * 128u;
     p.stage_bytes_b = (uint32_t)((info.tile_n / cg) * 128);
     p.flags = d.flags;

@@ -163,15 +163,20 @@ __device__ void mx_mma_issuer(const MxParams& q, uint8_t* ring, uint8_t* sf_ring
                     tmem_cp_scales<CG>(t_sfb + 8u * c, smem_desc_scale_slab(sf + 512u * (C + c)));
                     tmem_cp_scales<CG>(t_sfb + 8u * c + 4u, smem_desc_scale_slab(sf + 512u * (2 * C + c)));
                 }
-                const uint64_t da = smem_desc_sw128(sa);
-                const uint64_t db = smem_desc_sw128(sb);
+                // K-major: the next MMA is 32 bytes further along the 128-byte row (+2
+                // in the address field).  MN-major (8-bit only): 32 k-rows of 128 B on
+                // (+256), atoms along M/N one 128 x 128 box (16 KB) apart.
+                constexpr uint32_t kBox = 128u * 128u;
+                const uint64_t da = p.mn_major_a ? smem_desc_sw128_mn_lbo(sa, kBox) : smem_desc_sw128(sa);
+                const uint64_t db = p.mn_major_b ? smem_desc_sw128_mn_lbo(sb, kBox) : smem_desc_sw128(sb);
+                const uint64_t step_a = p.mn_major_a ? 256u : 2u;
+                const uint64_t step_b = p.mn_major_b ? 256u : 2u;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     int slab;
                     uint32_t sf_id;
                     mx_slab_of<KIND>(kk, slab, sf_id);
-                    // next MMA: 32 bytes further along the 128-byte row (+2 in the address field)
-                    mma_block_scaled<CG, KIND>(tmem_base, da + 2u * kk, db + 2u * kk,
+                    mma_block_scaled<CG, KIND>(tmem_base, da + step_a * kk, db + step_b * kk,
                                                idesc_with_scale_ids(p.idesc, sf_id), t_sfa + 4u * slab,
                                                t_sfb + 8u * slab, (kb != u.kb0 || kk != 0) ? 1u : 0u);
                 }

@@ -94,9 +94,12 @@ __device__ __forceinline__ void mma_block_scaled(uint32_t d_tmem, uint64_t a_des
 // Formats: mxf8f6f4 0 = E4M3, 1 = E5M2; mxf4 and mxf4nvf4 1 = E2M1.  The
 // scale-factor ids pick which byte (1X), byte pair (2X) or the whole word
 // (4X, id 0) of each 32-bit tensor-memory cell holds the MMA's scales.
+// The major bits may be 1 (MN-major) for 8-bit elements only.
 __host__ __device__ constexpr uint32_t make_idesc_block_scaled(uint32_t a_format, uint32_t b_format, uint32_t m,
-                                                               uint32_t n, uint32_t scale_ue8m0) {
-    return (a_format << 7) | (b_format << 10) | ((n >> 3) << 17) | (scale_ue8m0 << 23) | ((m >> 4) << 24);
+                                                               uint32_t n, uint32_t scale_ue8m0, uint32_t a_mn_major = 0,
+                                                               uint32_t b_mn_major = 0) {
+    return (a_format << 7) | (b_format << 10) | (a_mn_major << 15) | (b_mn_major << 16) | ((n >> 3) << 17) |
+           (scale_ue8m0 << 23) | ((m >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_with_scale_ids(uint32_t idesc, uint32_t sf_id) {
     return idesc | (sf_id << 29) | (sf_id << 4);

@@ -273,8 +273,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* D,
  * (kernel GEMM_KERNEL_MX): the tensor core applies the block scales inside
  * tcgen05.mma (.kind::mxf8f6f4 for 8-bit elements, .kind::mxf4 for MXFP4,
  * .kind::mxf4nvf4 for NVFP4), fp32 accumulation, one rounding to D's type.
- * A, B, D: device pointers laid out as at the top of this file (K-major A and
- * B; E2M1 rows a multiple of 32 elements apart, K even).  sf_a, sf_b: device
+ * A, B, D: device pointers laid out as at the top of this file (E4M3/E5M2 A
+ * and B in either majorness; E2M1 K-major, rows a multiple of 32 elements
+ * apart, K even).  sf_a, sf_b: device
  * pointers to the tiled scale bytes (16-byte aligned).  tensor_scales: NV: a
  * device pointer to two fp32 values {tA, tB}, read by the kernel when it runs;
  * MX: NULL.  Asynchronous and stream-ordered like gemm_run.

@@ -216,3 +216,27 @@ def test_random_shapes_bit_exact(case):
     32 (4-bit), either CTA group, every output type, capped grids."""
     prob = inputs.make(case["name"], dist="ints", seed=case["seed"], M=case["M"], N=case["N"], K=case["K"])
     check(prob, case["out"], exact=True, flags=case["cg"], max_ctas=case["ctas"])
+
+
+@pytest.mark.parametrize("cg_flag", [dg.GEMM_FLAG_CTA_GROUP_1, dg.GEMM_FLAG_CTA_GROUP_2])
+@pytest.mark.parametrize("mn_a,mn_b", [(True, False), (False, True), (True, True)])
+def test_mxfp8_mn_major_bit_exact(cg_flag, mn_a, mn_b):
+    """MXFP8 operands stored [k][m] (or [k][n]) reach the block-scaled MMA through
+    the descriptors' MN-major layout; the scales stay per row and K block."""
+    prob = inputs.make("mxfp8_8192", M=384, N=640, K=400, dist="ints", seed=59)
+    wl = prob.wl
+    A = prob.A.transpose(0, 1).contiguous() if mn_a else prob.A
+    B = prob.B.transpose(0, 1).contiguous() if mn_b else prob.B
+    D = torch.full((wl.M, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_F32,
+                        scale_mode=dg.GEMM_SCALE_MX_E8M0_32, flags=cg_flag,
+                        major_a=dg.GEMM_MN_MAJOR if mn_a else dg.GEMM_K_MAJOR,
+                        major_b=dg.GEMM_MN_MAJOR if mn_b else dg.GEMM_K_MAJOR)
+    with dg.Plan(desc) as plan:
+        plan.run_mx(A.cuda(), B.cuda(), D, prob.scale_a.cuda(), prob.scale_b.cuda())
+        assert plan.sync_status()[0] == dg.GEMM_OK
+    dref, _ = oracle.gemm(A, B, M=wl.M, N=wl.N, K=wl.K, dtype_a="e4m3", dtype_b="e4m3",
+                          major_a="mn" if mn_a else "k", major_b="mn" if mn_b else "k",
+                          scale_a=prob.scale_a, scale_b=prob.scale_b, scale_mode="mx")
+    assert np.array_equal(D.double().cpu().numpy(), dref[0])
+

@@ -53,13 +53,14 @@ def encoded(tmp_path_factory):
 #include "mx_ptx.cuh"
 using namespace dgb;
 int main() {
-    // (a_format, b_format, M, N, scale_ue8m0)
-    const unsigned cases[][5] = {{0, 0, 128, 256, 1}, {1, 0, 256, 256, 1}, {0, 1, 128, 128, 1},
-                                 {1, 1, 256, 256, 1}, {1, 1, 128, 256, 0}, {1, 1, 256, 256, 0}};
+    // (a_format, b_format, M, N, scale_ue8m0, a_mn_major, b_mn_major)
+    const unsigned cases[][7] = {{0, 0, 128, 256, 1, 0, 0}, {1, 0, 256, 256, 1, 0, 0}, {0, 1, 128, 128, 1, 0, 0},
+                                 {1, 1, 256, 256, 1, 0, 0}, {1, 1, 128, 256, 0, 0, 0}, {1, 1, 256, 256, 0, 0, 0},
+                                 {0, 0, 256, 256, 1, 1, 0}, {0, 1, 128, 256, 1, 0, 1}, {1, 0, 256, 256, 1, 1, 1}};
     for (auto& c : cases) {
-        unsigned base = make_idesc_block_scaled(c[0], c[1], c[2], c[3], c[4]);
-        for (unsigned id = 0; id < 4; ++id) printf("I %u %u %u %u %u %u %u\n", c[0], c[1], c[2], c[3], c[4], id,
-                                                    idesc_with_scale_ids(base, id));
+        unsigned base = make_idesc_block_scaled(c[0], c[1], c[2], c[3], c[4], c[5], c[6]);
+        for (unsigned id = 0; id < 4; ++id) printf("I %u %u %u %u %u %u %u %u %u\n", c[0], c[1], c[2], c[3], c[4],
+                                                    c[5], c[6], id, idesc_with_scale_ids(base, id));
     }
     const unsigned addrs[] = {0u, 1024u, 0x1F400u, 0x3FFF0u};
     for (unsigned a : addrs) printf("S %u %llu\n", a, (unsigned long long)smem_desc_scale_slab(a));
@@ -74,9 +75,9 @@ int main() {
 
 def test_block_scaled_instruction_descriptor(encoded):
     rows = [list(map(int, l.split()[1:])) for l in encoded if l.startswith("I ")]
-    assert len(rows) == 24
-    for fa, fb, m, n, ue8m0, sf_id, word in rows:
-        want = assemble(IDESC_FIELDS, {"a_format": fa, "b_format": fb, "a_major": 0, "b_major": 0,
+    assert len(rows) == 36
+    for fa, fb, m, n, ue8m0, ma, mb, sf_id, word in rows:
+        want = assemble(IDESC_FIELDS, {"a_format": fa, "b_format": fb, "a_major": ma, "b_major": mb,
                                        "n_dim": n >> 3, "scale_format": ue8m0, "m_dim": m >> 4,
                                        "a_sf_id": sf_id, "b_sf_id": sf_id})
         assert word == want, (fa, fb, m, n, ue8m0, sf_id, hex(word), hex(want))

@@ -47,7 +47,7 @@ def test_tensor_memory_bounds_the_nvfp4_ring():
     (dict(a=dg.GEMM_E4M3, b=dg.GEMM_E4M3, mode=dg.GEMM_SCALE_NV_E4M3_16), dg.GEMM_ERR_UNSUPPORTED),
     (dict(a=dg.GEMM_E4M3, b=dg.GEMM_E2M1, mode=dg.GEMM_SCALE_MX_E8M0_32), dg.GEMM_ERR_UNSUPPORTED),
     (dict(a=dg.GEMM_BF16, b=dg.GEMM_BF16, mode=dg.GEMM_SCALE_MX_E8M0_32), dg.GEMM_ERR_UNSUPPORTED),
-    (dict(a=dg.GEMM_E4M3, b=dg.GEMM_E4M3, mode=dg.GEMM_SCALE_MX_E8M0_32, major_b=dg.GEMM_MN_MAJOR),
+    (dict(a=dg.GEMM_E2M1, b=dg.GEMM_E2M1, mode=dg.GEMM_SCALE_MX_E8M0_32, major_b=dg.GEMM_MN_MAJOR),
      dg.GEMM_ERR_UNSUPPORTED),
     (dict(a=dg.GEMM_E4M3, b=dg.GEMM_E4M3, mode=dg.GEMM_SCALE_MX_E8M0_32, tile_n=128), dg.GEMM_ERR_UNSUPPORTED),
     (dict(a=dg.GEMM_E4M3, b=dg.GEMM_E4M3, mode=dg.GEMM_SCALE_MX_E8M0_32, ld_sa=4), dg.GEMM_ERR_INVALID_ARG),
@@ -80,3 +80,12 @@ def test_work_units_cover_every_tile_once():
             seen.append(u.tile)
             i += 1
     assert sorted(seen) == list(range(info.num_tiles))
+
+
+def test_mn_major_mxfp8_is_planned():
+    """8-bit MX operands may be MN-major (packed E2M1 may not)."""
+    for ma, mb in [(dg.GEMM_MN_MAJOR, dg.GEMM_K_MAJOR), (dg.GEMM_K_MAJOR, dg.GEMM_MN_MAJOR),
+                   (dg.GEMM_MN_MAJOR, dg.GEMM_MN_MAJOR)]:
+        st, info = plan(4096, 4096, 4096, dg.GEMM_E4M3, major_a=ma, major_b=mb)
+        assert st == dg.GEMM_OK and info.kernel == dg.GEMM_KERNEL_MX
+
