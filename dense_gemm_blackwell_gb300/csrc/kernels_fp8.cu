@@ -312,24 +312,34 @@ __global__ void __launch_bounds__(kFp8Threads, 1) fp8_block_kernel(const __grid_
             for (int c = 0; c < kChunks; ++c) {
                 const int x = col0 + c * kChunkCols;
                 if (x >= p.N) break;
+                // 16-byte piece j of this thread's row, packed straight from the accumulators
+                auto piece = [&](int j) -> uint4 {
+                    if constexpr (OUT == GEMM_F32) {
+                        const int e = c * 32 + 4 * j;
+                        return make_uint4(__float_as_uint(acc[e]), __float_as_uint(acc[e + 1]),
+                                          __float_as_uint(acc[e + 2]), __float_as_uint(acc[e + 3]));
+                    } else {
+                        const int e = c * 64 + 8 * j;
+                        return make_uint4(pack2<OUT>(acc[e], acc[e + 1]), pack2<OUT>(acc[e + 2], acc[e + 3]),
+                                          pack2<OUT>(acc[e + 4], acc[e + 5]), pack2<OUT>(acc[e + 6], acc[e + 7]));
+                    }
+                };
+                if (chunk_needs_clipped_store<kOutBytes>(x, kChunkCols, p.N)) {
+                    // ragged right edge inside a 16-byte granule: plain stores up to N
+                    const int row = m_warp + lane;
+                    if (row < p.M)
+                        store_segment_clipped<kOutBytes>(static_cast<uint8_t*>(p.d_ptr) +
+                                                             ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) *
+                                                                 kOutBytes,
+                                                         p.N - x, piece);
+                    continue;
+                }
                 // single staging buffer: the previous store must have read it
                 if (lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
-                // 16-byte piece j of this thread's row, packed straight from the accumulators
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 q;
-                    if constexpr (OUT == GEMM_F32) {
-                        const int e = c * 32 + 4 * j;
-                        q = make_uint4(__float_as_uint(acc[e]), __float_as_uint(acc[e + 1]),
-                                       __float_as_uint(acc[e + 2]), __float_as_uint(acc[e + 3]));
-                    } else {
-                        const int e = c * 64 + 8 * j;
-                        q = make_uint4(pack2<OUT>(acc[e], acc[e + 1]), pack2<OUT>(acc[e + 2], acc[e + 3]),
-                                       pack2<OUT>(acc[e + 4], acc[e + 5]), pack2<OUT>(acc[e + 6], acc[e + 7]));
-                    }
-                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = q;
-                }
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = piece(j);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

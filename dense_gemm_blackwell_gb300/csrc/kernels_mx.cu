@@ -349,6 +349,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_kernel(const __grid_constant
                         }
                     };
                     const int x = n0 + (c0 + cc) * kChunkCols;
+                    if (chunk_needs_clipped_store<kOutBytes>(x, kChunkCols, p.N)) {
+                        // ragged right edge inside a 16-byte granule: plain stores up to N
+                        const int row = m0 + lane;
+                        if (row < p.M)
+                            store_segment_clipped<kOutBytes>(static_cast<uint8_t*>(p.d_ptr) +
+                                                                 ((size_t)b * p.stride_d + (size_t)row * p.ldd + x) *
+                                                                     kOutBytes,
+                                                             p.N - x, piece);
+                        continue;
+                    }
                     if (lane == 0) bulk_wait_group_read<0>();
                     __syncwarp();
 #pragma unroll

@@ -500,8 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                             }
                         };
                         const int x = n0 + c * kChunkCols;
-                        if (p.direct_store) {
-                            // This thread's row: 128 contiguous bytes, streaming stores.
+                        if (p.direct_store || chunk_needs_clipped_store<kOutBytes>(x, kChunkCols, p.N)) {
+                            // This thread's row: 128 contiguous bytes, streaming stores
+                            // (element by element past N at a ragged right edge).
                             const int row = m0 + lane;
                             if (row < p.M) {
                                 uint8_t* dst = static_cast<uint8_t*>(p.d_ptr) +
@@ -510,23 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
 #pragma unroll
                                     for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<uint4*>(dst) + j, piece(j));
                                 } else {
-                                    // ragged right edge: element by element, up to N
-                                    const int valid = p.N - x;
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j) {
-                                        const uint4 q = piece(j);
-#pragma unroll
-                                        for (int k = 0; k < 4; ++k) {
-                                            const uint32_t wv_k = k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
-                                            if constexpr (OUT == GEMM_F32) {
-                                                if (4 * j + k < valid) reinterpret_cast<uint32_t*>(dst)[4 * j + k] = wv_k;
-                                            } else {
-                                                const int e0 = 8 * j + 2 * k;
-                                                if (e0 < valid) reinterpret_cast<uint16_t*>(dst)[e0] = (uint16_t)(wv_k & 0xFFFFu);
-                                                if (e0 + 1 < valid) reinterpret_cast<uint16_t*>(dst)[e0 + 1] = (uint16_t)(wv_k >> 16);
-                                            }
-                                        }
-                                    }
+                                    store_segment_clipped<kOutBytes>(dst, p.N - x, piece);
                                 }
                             }
                             continue;

@@ -56,6 +56,40 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Whether an output chunk is written with plain stores rather than a TMA
+// store: a TMA store writes whole 16-byte granules of a row, so a chunk that
+// ends inside one (N x element bytes not a multiple of 16, with the caller's
+// padding columns behind column N) would also overwrite that padding.
+template <int kOutBytes>
+__device__ __forceinline__ bool chunk_needs_clipped_store(int x, int chunk_cols, int N) {
+    return x + chunk_cols > N && ((N * kOutBytes) & 15) != 0;
+}
+
+// One thread's 128-byte segment of an output row (eight 16-byte pieces,
+// piece(j)) at dst, of which the first `valid` elements lie inside D: whole
+// pieces while they fit, then element by element up to column N.  dst is
+// 16-byte aligned.
+template <int kOutBytes, typename Piece>
+__device__ __forceinline__ void store_segment_clipped(uint8_t* dst, int valid, Piece&& piece) {
+    constexpr int kPer = 16 / kOutBytes;   // elements per piece
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j * kPer >= valid) break;
+        const uint4 q = piece(j);
+        if ((j + 1) * kPer <= valid) {
+            *reinterpret_cast<uint4*>(dst + 16 * j) = q;
+        } else {
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                if (j * kPer + e >= valid) break;
+                if constexpr (kOutBytes == 4) reinterpret_cast<uint32_t*>(dst + 16 * j)[e] = w[e];
+                else reinterpret_cast<uint16_t*>(dst + 16 * j)[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+            }
+        }
+    }
+}
+
 // Copy one operand's slice for one ring stage: `rows` rows (M or N) of
 // `tile_k` K elements.  K-major: ATOMS boxes of (tile_k / ATOMS) x rows, one
 // 128-byte swizzle atom column each, `atom_stride` bytes apart (default
