@@ -406,7 +406,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     if ((d.flags & GEMM_FLAG_STAGE_K2) && (mn_a || mn_b)) return GEMM_ERR_UNSUPPORTED;
     const int64_t atom_k = 128 / elem_bytes(d.dtype_a);
     const int64_t atom_bytes = 128 * 128 + (tile_n / cg) * 128;   // A and B, one atom of K
-    const int64_t fixed_bytes = kStagingBytes + 8 * (3 * tmem_stages + 1) + 8 + kAlignSlack;
+    const int64_t fixed_bytes = kStagingBytes + 8 * (4 * tmem_stages + 1) + 8 + kAlignSlack;
     int atoms = 1;
     if (d.flags & GEMM_FLAG_STAGE_K2) {
         atoms = 2;
@@ -423,7 +423,7 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     // smem buys nothing as a 7th ring stage at 8192^3 (within 1 %), and TMA
     // stores are faster at 4096^3 (+2 %) and on batched problems (+23 %).
     auto smem_for_mode = [&](int64_t s, bool direct) {
-        return s * stage_bytes + (direct ? 0 : kStagingBytes) + 8 * (2 * s + 3 * tmem_stages + 1) + 8 + kAlignSlack;
+        return s * stage_bytes + (direct ? 0 : kStagingBytes) + 8 * (2 * s + 4 * tmem_stages + 1) + 8 + kAlignSlack;
     };
     auto max_stages = [&](bool direct) {
         int64_t s = 16;

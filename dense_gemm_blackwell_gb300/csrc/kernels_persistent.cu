@@ -27,8 +27,11 @@
 // Tiles up to 256 wide keep two accumulators in tensor memory, so the
 // epilogue of tile t overlaps the MMAs of tile t+1.  512-wide tiles (two
 // N = 256 MMAs per K step) fill all 512 columns with one accumulator, handed
-// back in two 256-column halves: the MMAs of tile t+1 start on the left half
-// and wait for the right one after kWideLeadStages stages.  The grid is
+// back in two 256-column halves.  A long enough tile runs its first K blocks
+// on the left half alone and repeats them on the right half alone at its end
+// (split units, units.cuh), so each half drains while MMAs run on the other;
+// otherwise the MMAs of tile t+1 start on the left half and wait for the
+// right one after kWideLeadStages stages.  The grid is
 // persistent: CTA (pair) c takes tiles c, c+G, ... in a grouped raster that
 // keeps a wave's A and B panels in L2; when the tiles do not fill whole waves,
 // a stream-K region split along K comes first (units.cuh).  Every thread
@@ -91,7 +94,7 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
     const uint64_t tmo = p.timeout_ns;
     auto full = [&](int s) { return full0 + 8u * s; };
     auto empty = [&](int s) { return empty0 + 8u * s; };
-    auto tfull = [&](int a) { return tfull0 + 8u * a; };
+    auto tfull = [&](int a, int part) { return tfull0 + 8u * (2 * a + part); };
     auto tempty = [&](int a, int part) { return tempty0 + 8u * (2 * a + part); };
     const uint64_t b_atom = (uint64_t)(p.tile_n / CG) * 8u;   // B atom stride in descriptor units
     int stage = 0;
@@ -110,8 +113,10 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
             break;
         }
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.tile_n);
-        // The MMAs of one ring stage for accumulator halves [h0, h1); issuer lane only.
-        auto issue_stage = [&](int st, int kb, int h0, int h1) {
+        // The MMAs of one ring stage for accumulator halves [h0, h1), the first
+        // of the left (right) half's MMAs overwriting it if first_l (first_r);
+        // issuer lane only.
+        auto issue_stage = [&](int st, int h0, int h1, bool first_l, bool first_r) {
             tc_fence_after();
             const uint32_t sa = smem_u32(ring + (size_t)st * stage_bytes);
             const uint32_t sb = sa + p.stage_bytes_a;
@@ -126,10 +131,10 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                 // next atom: 128 rows (A) or tile_n / CG rows (B) x 128 B on
                 const uint64_t da_at = da + (uint64_t)at * (128u * 8u);
                 const uint64_t db_at = db + (uint64_t)at * b_atom;
-                const bool first = kb == u.kb0 && at == 0;
 #pragma unroll
                 for (int h = 0; h < HALVES; ++h) {
                     if (h < h0 || h >= h1) continue;
+                    const bool first = (h == 0 ? first_l : first_r) && at == 0;
                     const uint32_t d_h = d_tmem + (uint32_t)(h * 256);
                     const uint64_t db_h = db_at + (uint64_t)(h * (256 / CG) * 8);
                     if (p.mma_kind == kMmaKindTF32) {
@@ -147,9 +152,41 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
         };
         int kb = u.kb0;
         if constexpr (HALVES == 2) {
+            const int n = u.kb1 - u.kb0;
+            const int L = split_stages(u, true);
+            if (L > 0) {
+                // Split unit (units.cuh): left-only stages, then both halves once
+                // the right one is free, then right-only stages; the left half is
+                // complete (and handed to the epilogue) after the last two-half stage.
+                for (int i = 0; i < n + L; ++i) {
+                    int walk, halves;
+                    stage_of(i, n, L, walk, halves);
+                    if (i == L && !wait_phase_warp<CG == 2>(tempty(acc, 1), acc_phase ^ 1u, abort_flag, tmo, p.status,
+                                                           kRoleMma, acc, t)) {
+                        aborted = true;
+                        break;
+                    }
+                    if (!wait_phase_warp<false>(full(stage), phase, abort_flag, tmo, p.status, kRoleMma, stage, t)) {
+                        aborted = true;
+                        break;
+                    }
+                    if (issuer) {
+                        issue_stage(stage, (halves & kHalfLeft) ? 0 : 1, (halves & kHalfRight) ? 2 : 1, i == 0, i == L);
+                        commit_to<CG>(empty(stage));
+                        if (i == n - 1) commit_to<CG>(tfull(acc, 0));
+                    }
+                    __syncwarp();
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (aborted) break;
+                if (issuer) commit_to<CG>(tfull(acc, 1));
+                __syncwarp();
+                if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
+                continue;
+            }
             // The epilogue hands back columns [0, 256) first: run the first
             // stages' left-half MMAs while it still reads [256, 512).
-            const int lead = min(kWideLeadStages, u.kb1 - u.kb0);
+            const int lead = min(kWideLeadStages, n);
             int st = stage;
             uint32_t ph = phase;
             for (int i = 0; i < lead; ++i) {
@@ -157,7 +194,7 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                     aborted = true;
                     break;
                 }
-                if (issuer) issue_stage(st, u.kb0 + i, 0, 1);
+                if (issuer) issue_stage(st, 0, 1, i == 0, false);
                 __syncwarp();
                 if (++st == S) { st = 0; ph ^= 1u; }
             }
@@ -169,7 +206,7 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
             }
             if (issuer) {
                 for (int i = 0, st2 = stage; i < lead; ++i) {
-                    issue_stage(st2, u.kb0 + i, 1, 2);
+                    issue_stage(st2, 1, 2, false, i == 0);
                     commit_to<CG>(empty(st2));
                     if (++st2 == S) st2 = 0;
                 }
@@ -185,14 +222,17 @@ __device__ __forceinline__ void mma_issuer(const PersistentParams& p, uint8_t* r
                 break;
             }
             if (issuer) {
-                issue_stage(stage, kb, 0, HALVES);
+                issue_stage(stage, 0, HALVES, kb == u.kb0, kb == u.kb0);
                 commit_to<CG>(empty(stage));
             }
             __syncwarp();
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
-        if (issuer) commit_to<CG>(tfull(acc));
+        if (issuer) {
+            commit_to<CG>(tfull(acc, 0));
+            if (HALVES == 2) commit_to<CG>(tfull(acc, 1));
+        }
         __syncwarp();
         if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
     }
@@ -218,17 +258,19 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
     uint8_t* ring = smem;
     uint8_t* staging = ring + (size_t)S * stage_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + (p.direct_store ? 0 : kEpilogueWarps * kStagingBytes));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3 * TS + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4 * TS + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8u * S;
+    // accumulator full / empty: two of each per accumulator, one per part
+    // (columns [0, 256) and [256, 512); tiles up to 256 wide use part 0 only)
     const uint32_t tfull0 = empty0 + 8u * S;
-    const uint32_t tempty0 = tfull0 + 8u * TS;        // two per accumulator: columns [0, 256), [256, 512)
+    const uint32_t tempty0 = tfull0 + 16u * TS;
     const uint32_t drain_bar = tempty0 + 16u * TS;
     auto full = [&](int s) { return full0 + 8u * s; };
     auto empty = [&](int s) { return empty0 + 8u * s; };
-    auto tfull = [&](int a) { return tfull0 + 8u * a; };
+    auto tfull = [&](int a, int part) { return tfull0 + 8u * (2 * a + part); };
     auto tempty = [&](int a, int part) { return tempty0 + 8u * (2 * a + part); };
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
@@ -242,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             mbar_init(empty(s), 1);
         }
         for (int a = 0; a < TS; ++a) {
-            mbar_init(tfull(a), 1);
+            mbar_init(tfull(a, 0), 1);
+            mbar_init(tfull(a, 1), 1);
             mbar_init(tempty(a, 0), CG * kEpilogueWarps);
             mbar_init(tempty(a, 1), CG * kEpilogueWarps);
         }
@@ -352,10 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const int t = u.tile;
             int b, mb, nb;
             tile_coords(p, t, b, mb, nb);
-            const bool ok = wait_phase_warp<false>(tfull(acc), acc_phase, abort_flag, tmo, p.status, kRoleEpilogue,
-                                                   acc, t);
+            const bool ok = wait_phase_warp<false>(tfull(acc, 0), acc_phase, abort_flag, tmo, p.status,
+                                                   kRoleEpilogue, acc, t);
             if (!ok) break;
             tc_fence_after();
+            // A 512-wide tile's right part may complete after its left one
+            // (split units, units.cuh): wait for it before reading it.
+            auto wait_part = [&](int pt) {
+                if (pt == 0) return true;
+                const bool got = wait_phase_warp<false>(tfull(acc, pt), acc_phase, abort_flag, tmo, p.status,
+                                                        kRoleEpilogue, acc, t);
+                tc_fence_after();
+                return got;
+            };
+            bool lost = false;
             const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * p.tile_n);
             const int m0 = mb * (128 * CG) + (int)rank * 128 + wq * 32;
             const int n0 = nb * p.tile_n;
@@ -377,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                 // this warp's last TMEM load of it, before that load's stores.
                 float4* part = reinterpret_cast<float4*>(p.sk_partials) + part_base;
                 for (int pt = 0; pt < parts; ++pt) {
+                    if (!wait_part(pt)) {
+                        lost = true;
+                        break;
+                    }
                     const int q_lo = (pt * cpp + (half == 0 ? 0 : split)) * kSub;   // this warp's 32-column loads
                     const int q_hi = (pt * cpp + (half == 0 ? split : cpp)) * kSub;
                     if (q_lo >= q_hi) release(pt);
@@ -393,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                     }
                 }
+                if (lost) break;
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) store_release_gpu(flag, sk_launch_epoch(p.sk_epoch));
@@ -429,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             // rest of the tile (padding beyond M or N) is neither read nor stored.
             const int n_valid = (m0 < p.M) ? min(nchunks, (p.N - n0 + kChunkCols - 1) / kChunkCols) : 0;
             for (int pt = 0; pt < parts; ++pt) {
+                if (!wait_part(pt)) {
+                    lost = true;
+                    break;
+                }
                 const int c_lo = pt * cpp + (half == 0 ? 0 : split);          // this warp's chunks of the part
                 const int c_end = min(pt * cpp + (half == 0 ? split : cpp), n_valid);
                 if (c_lo >= c_end) release(pt);
@@ -538,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                     c0 += nc;
                 }
             }
+            if (lost) break;
             if (++acc == TS) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) bulk_wait_group<0>();

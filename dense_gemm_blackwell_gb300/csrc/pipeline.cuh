@@ -182,7 +182,13 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
         tile_coords(p, t, b, mb, nb);
         const int a_row = mb * (128 * CG) + (int)rank * 128;
         const int b_row = nb * p.tile_n + (int)rank * b_rows;
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        // 512-wide tiles: the unit's stages, split ones included (units.cuh)
+        const int n = u.kb1 - u.kb0;
+        const int L = split_stages(u, HALVES == 2);
+        for (int i = 0; i < n + L; ++i) {
+            int walk, halves;
+            stage_of(i, n, L, walk, halves);
+            const int kb = u.kb0 + walk;
             if (!wait_phase_warp<false, true>(empty0 + 8u * stage, phase ^ 1u, abort_flag, tmo, p.status,
                                               kRoleProducer, stage, t)) {
                 aborted = true;
@@ -191,7 +197,12 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
             const uint32_t fb = fb0 + 8u * stage;
             const bool drop = drop_any && issued == 0;
             if (elect_one()) {
-                if (leader && (parts & kPartA) != 0) mbar_arrive_expect_tx(full0 + 8u * stage, tx_bytes);
+                if (leader && (parts & kPartA) != 0) {
+                    // a split stage carries one of B's two halves
+                    const uint32_t tx = halves == kHalvesBoth ? tx_bytes
+                                                              : tx_bytes - (uint32_t)CG * (p.stage_bytes_b / 2u);
+                    mbar_arrive_expect_tx(full0 + 8u * stage, tx);
+                }
                 if (!drop) {
                     const uint32_t sa = smem_u32(ring + (size_t)stage * stage_bytes);
                     const uint32_t sb = sa + p.stage_bytes_a;
@@ -209,7 +220,7 @@ __device__ void producer_loop(const PersistentParams& p, uint8_t* ring, uint32_t
                         constexpr int kHalfRows = 256 / CG;
 #pragma unroll
                         for (int h = 0; h < HALVES; ++h)
-                            if ((parts & (kPartB0 << h)) != 0)
+                            if ((parts & (kPartB0 << h)) != 0 && (halves & (1 << h)) != 0)
                                 load_operand<CG, ATOMS>(sb + (uint32_t)(h * kHalfRows * 128), &p.tmap_b, fb, false,
                                                         kHalfRows, nb * p.tile_n + h * 256 + (int)rank * kHalfRows,
                                                         kx, b, p.batched != 0, false, pol_a, atom_k,

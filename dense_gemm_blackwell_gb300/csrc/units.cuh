@@ -82,4 +82,38 @@ __host__ __device__ __forceinline__ bool next_unit(const PersistentParams& p, in
     return true;
 }
 
+// 512-wide tiles hold one accumulator of two 256-column halves, and the next
+// tile can start only on a half the epilogue has drained.  A whole unit of
+// such a tile therefore runs its first kSplitStages K blocks for the left half
+// alone and repeats them for the right half alone after its last K block: the
+// left half is complete kSplitStages stages before the right one, so it
+// drains while the tile's right-only stages run, and the right half drains
+// while the next tile's left-only stages run.  Those stages carry A and one
+// half of B.  Units with fewer than 4 x kSplitStages K blocks run every stage
+// on both halves.  Six split stages measured best on GB300 (8192^3 and 4096^3
+// bf16, 2 % faster than none; from eight on, the extra half-stages, which take
+// in A and half of B per 512 MMA cycles, cost more than the hidden drain).
+constexpr int kSplitStages = 6;
+
+__host__ __device__ __forceinline__ int split_stages(const WorkUnit& u, bool wide) {
+    return (wide && u.role == kUnitWhole && u.kb1 - u.kb0 >= 4 * kSplitStages) ? kSplitStages : 0;
+}
+
+// Stage i (0 <= i < n + L) of a unit of n K blocks with L split stages: the
+// position of its K block in the unit's walk, and the accumulator halves it
+// feeds (bit 0: left, bit 1: right).
+constexpr int kHalfLeft = 1, kHalfRight = 2, kHalvesBoth = 3;
+__host__ __device__ __forceinline__ void stage_of(int i, int n, int L, int& walk, int& halves) {
+    if (i < L) {
+        walk = i;
+        halves = kHalfLeft;
+    } else if (i < n) {
+        walk = i;
+        halves = kHalvesBoth;
+    } else {
+        walk = i - n;
+        halves = kHalfRight;
+    }
+}
+
 }  // namespace dgb

@@ -141,6 +141,24 @@ def test_wide_tiles_bit_exact(cg_flag, dtype_in, out, epi):
     assert r["ok"], (r, info)
 
 
+@pytest.mark.parametrize("cg_flag,max_ctas", [(dg.GEMM_FLAG_CTA_GROUP_1, 5), (dg.GEMM_FLAG_CTA_GROUP_2, 6)])
+@pytest.mark.parametrize("K", [1472, 1536, 1560])
+def test_wide_tiles_split_schedule_bit_exact(cg_flag, max_ctas, K):
+    """A 512-wide whole tile of at least 24 K blocks runs its first six K
+    blocks for the left accumulator half alone and repeats them for the right
+    half after its last one: K = 1472 is 23 blocks (no split), 1536 is 24 and
+    1560 is 25 with a ragged last block.  Four tiles per cluster (max_ctas),
+    so every other tile walks K backwards and each tile's split stages follow
+    the previous tile's."""
+    prob = inputs.make("square8192_bf16", M=520, N=2048, K=K, dist="ints", seed=77)
+    got, dref, s, info = run(prob, "f32", flags=cg_flag, tile_n=512, max_ctas=max_ctas)
+    assert info["tile_n"] == 512 and info["num_tiles"] == 4 * info["grid"] // info["cta_group"]
+    r = compare(got, dref, s, "f32", TOL_TF32, exact=True)
+    if not r["ok"]:
+        dump_on_failure("wide_split_K%d_cg%d" % (K, info["cta_group"]), got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+
+
 @pytest.mark.parametrize("epi", [dg.GEMM_FLAG_EPILOGUE_TMA, dg.GEMM_FLAG_EPILOGUE_DIRECT])
 def test_wide_tiles_stream_k_random(epi):
     """512-wide pair tiles with stream-K (sampled rows of every tile row band)."""
