@@ -58,19 +58,6 @@
 
 namespace dgb {
 
-// Move registers between the warpgroups of a CTA (every thread of the
-// warpgroup executes it).  The pool is what the CTA was launched with
-// (threads x registers per thread): an increase waits until other
-// warpgroups' decreases leave room, so callers keep the shares within it.
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // acc[0..1] += x[0..1] * s with one packed fp32 FMA (round to nearest, as two fmaf)
 __device__ __forceinline__ void fma2_rn(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
     asm("{\n\t.reg .b64 a, x, s;\n\t"

@@ -20,8 +20,8 @@
 //                256 rows; every CTA of a pair holds B's scales in full, since
 //                each SM's tensor core applies them to its 128 rows of D);
 //                posts the scale bytes on the same full barrier
-//   warps 4..11: epilogue: tcgen05.ld of the accumulator, hand-back, convert
-//                (times tA * tB for NVFP4), stage, TMA store
+//   warps 4..11: epilogue: tcgen05.ld of all of a warp's accumulator columns,
+//                hand-back, convert (times tA * tB for NVFP4), stage, TMA store
 //
 // Tensor memory: one 256-column fp32 accumulator (columns [0, 256)) and, from
 // column 256, one scale slot per ring stage (A's slabs, then B's, 4 columns
@@ -49,6 +49,17 @@ constexpr int kMxThreads = 32 * (kMxEpiWarp0 + kMxEpiWarps);
 constexpr uint32_t kMxStagingBytes = 32 * 128;   // one warp's output chunk: 32 rows x 128 B
 constexpr int kMxTileN = 256;
 constexpr int kMxSfCol0 = 256;                   // first tensor-memory column of the scale slots
+// Registers: an epilogue warp reads all its columns of the accumulator (128
+// per thread) before handing it back, so the next tile's MMAs wait only for
+// the tcgen05.ld, not for the TMA stores behind it.  Twelve warps launch with
+// 168 registers each; the first warpgroup (producers, MMA) gives registers
+// back (setmaxnreg) down to kMxRegsLow and the two epilogue warpgroups take
+// them up to kMxRegsHigh.
+constexpr int kMxLaunchRegs = 168;
+constexpr int kMxRegsLow = 56;
+constexpr int kMxRegsHigh = 224;
+static_assert(128 * kMxRegsLow + 32 * kMxEpiWarps * kMxRegsHigh <= kMxThreads * kMxLaunchRegs,
+              "register shares exceed the launch's pool");
 
 // Scale slab and scale-factor id of MMA kk (0..3) of a 128-byte K atom.
 // mxf8f6f4: K32 per MMA, one E8M0 per 32 -> slab 0, byte kk.
@@ -206,7 +217,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_kernel(const __grid_constant
     constexpr int kChunks = kMxTileN / kChunkCols;        // chunks per tile row: 8 (fp32) or 4
     constexpr int kWarpChunks = kChunks / 2;              // per epilogue warp (two warps per lane quarter)
     constexpr int kSub = kChunkCols / 32;                 // 32-column TMEM loads per chunk
-    constexpr int kBatchChunks = OUT == GEMM_F32 ? 2 : 1; // chunks held in registers at once
+    constexpr int kBatchChunks = kWarpChunks;             // a warp's chunks, all held in registers at once
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,23 +277,29 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_kernel(const __grid_constant
     const int num_clusters = gridDim.x / CG;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        producer_loop<CG, 1, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
-                                        num_clusters);
-        __syncwarp();
-    } else if (warp == 2) {
-        producer_loop<CG, 1, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank, cluster_id,
-                                         num_clusters);
-        __syncwarp();
-    } else if (warp == 3) {
-        mx_scale_producer<CG>(q, sf_ring, full0, empty0, abort_flag, rank, cluster_id, num_clusters);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (leader)
-            mx_mma_issuer<CG, KIND>(q, ring, sf_ring, stage_bytes, tmem_base, full0, empty0, tfull, tempty, drain_bar,
-                                    abort_flag, cluster_id, num_clusters);
-        __syncwarp();
+    // Each role raises or lowers its registers first thing, so that the code
+    // that follows is compiled against its own share.
+    if (warp < kMxEpiWarp0) {
+        setmaxnreg_dec<kMxRegsLow>();
+        if (warp == 0) {
+            producer_loop<CG, 1, 1, kPartA>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                            cluster_id, num_clusters);
+            __syncwarp();
+        } else if (warp == 2) {
+            producer_loop<CG, 1, 1, kPartB0>(p, ring, stage_bytes, p.tile_k, full0, empty0, abort_flag, rank,
+                                             cluster_id, num_clusters);
+            __syncwarp();
+        } else if (warp == 3) {
+            mx_scale_producer<CG>(q, sf_ring, full0, empty0, abort_flag, rank, cluster_id, num_clusters);
+            __syncwarp();
+        } else {
+            if (leader)
+                mx_mma_issuer<CG, KIND>(q, ring, sf_ring, stage_bytes, tmem_base, full0, empty0, tfull, tempty,
+                                        drain_bar, abort_flag, cluster_id, num_clusters);
+            __syncwarp();
+        }
     } else {
+        setmaxnreg_inc<kMxRegsHigh>();
         // ------------------------------------------------------------ epilogue
         const bool stream_d = (p.l2_hints & kHintStreamD) != 0;
         const uint64_t pol_d = l2_policy_evict_first();
@@ -407,9 +424,20 @@ static cudaLaunchConfig_t mx_config(size_t smem, int grid, cudaStream_t stream, 
     return cfg;
 }
 
+// The kernel's setmaxnreg shares assume it was built with kMxLaunchRegs
+// registers per thread: with fewer the epilogue warps' increase could never
+// be granted, so such a build is refused rather than launched.
+template <typename Kern>
+static bool mx_regs_ok(Kern kern) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kern) != cudaSuccess) return false;
+    return a.numRegs == kMxLaunchRegs;
+}
+
 template <int CG, int OUT, int KIND>
 static cudaError_t mx_launch_typed(const MxParams& q, int grid, size_t smem, cudaStream_t stream) {
     auto kern = mx_kernel<CG, OUT, KIND>;
+    if (!mx_regs_ok(kern)) return cudaErrorInvalidConfiguration;
     static std::atomic<int> smem_set[kMaxDevices];
     cudaError_t e = ensure_smem_limit(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
@@ -424,6 +452,7 @@ static cudaError_t mx_launch_typed(const MxParams& q, int grid, size_t smem, cud
 template <int CG, int OUT, int KIND>
 static int mx_clusters_typed(size_t smem) {
     auto kern = mx_kernel<CG, OUT, KIND>;
+    if (!mx_regs_ok(kern)) return 0;
     static std::atomic<int> smem_set[kMaxDevices];
     if (ensure_smem_limit(kern, smem, smem_set) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];

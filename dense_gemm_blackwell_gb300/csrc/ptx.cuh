@@ -268,6 +268,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
 
+// Move registers between the warpgroups of a CTA (every thread of the
+// warpgroup executes it).  The pool is what the CTA was launched with
+// (threads x registers per thread): an increase waits until other
+// warpgroups' decreases leave room, so callers keep the shares within it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 template <int CG>
