@@ -15,7 +15,9 @@ the data path); the elapsed time is the maximum over ranks.
 After the headline, the same run times every other workload of the suite
 (single-CTA example, 4096^3, batched 512 x 256^3, fp32-block-scaled e4m3,
 MXFP8, MXFP4, NVFP4) with its own launches, CUDA events, clock samples and
-roofline, reported under "other_workloads" on the same JSON line.
+roofline, reported under "other_workloads" on the same JSON line; then
+torch.matmul (cuBLAS) on the 16-bit shapes, as context only
+("library_context"), off this library's measured path.
 
 --impl reference times the CPU oracle (the plain fp64 triple loop) on this
 host's cores on a bounded sample of the same workload (rank 0 only).
@@ -517,6 +519,44 @@ def measure_other(dg, torch, name, sampler, sm_count, target_ms=200.0):
     return entry
 
 
+def library_context(torch, target_ms=100.0):
+    """torch.matmul (a vendor library) on the 16-bit workloads' shapes, timed
+    like the other workloads: context for the numbers above, not this
+    library's path.  torch.matmul of bf16 / f16 operands returns bf16 / f16,
+    so the 8192^3 entry has a 16-bit output where the headline writes fp32."""
+    g = torch.Generator(device="cuda").manual_seed(9)
+    out = {}
+    for key, (batch, n, dt) in {"square8192_bf16_out_bf16": (1, 8192, torch.bfloat16),
+                                "square4096_bf16": (1, 4096, torch.bfloat16),
+                                "batched256_f16": (512, 256, torch.float16)}.items():
+        shape = (batch, n, n) if batch > 1 else (n, n)
+        A = torch.rand(shape, generator=g, device="cuda").to(dt)
+        B = torch.rand(shape, generator=g, device="cuda").to(dt)
+        step = lambda: torch.matmul(A, B.transpose(-1, -2))  # noqa: E731
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        launches = int(min(5000, max(10, target_ms / max(e0.elapsed_time(e1), 1e-3))))
+        e0.record()
+        for _ in range(launches):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / launches
+        flop = 2.0 * batch * n ** 3
+        byts = 3.0 * batch * n * n * A.element_size()
+        out[key] = {"ms_per_launch": ms, "TFLOP/s": flop / ms / 1e9, "GB/s": byts / ms / 1e6, "launches": launches}
+        del A, B
+    torch.cuda.empty_cache()
+    out["note"] = "torch.matmul (cuBLAS) on the same shapes; context only, off this library's measured path"
+    return out
+
+
 def run_ours(args):
     import torch
     import dense_gemm_blackwell_gb300 as dg
@@ -693,6 +733,7 @@ def run_ours(args):
             others[name] = measure_other(dg, torch, name, sampler, sm_count)
         sampler.stop()
         line["other_workloads"] = others
+        line["library_context"] = library_context(torch)
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()

@@ -139,7 +139,7 @@ def test_stream_k_region_256_wide():
 
 def test_stream_k_only():
     """80 tiles of 256 x 512 on 76 pairs: every tile is in the stream-K region."""
-    desc, info = plan(2048, 5120, 2048, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
+    desc, info = plan(2048, 5120, 2048, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, tile_n=512)
     assert info.stream_k_tiles == info.num_tiles == 80
     sched = check_schedule(desc, info)
     assert all(u["tile"] >= 0 for lst in sched.values() for u in lst)
