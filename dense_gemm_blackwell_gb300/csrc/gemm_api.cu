@@ -45,7 +45,6 @@ constexpr int kSkFlagsPerCta = 8;         // stream-K: one published flag per ep
 constexpr size_t kSkEpochOffset = 128;
 static_assert(sizeof(gemm_device_error_t) <= kSkEpochOffset, "error record overlaps the launch counter");
 constexpr int64_t kStagingBytes = 8 * 32 * 128;   // 8 epilogue warps x one 4 KB buffer
-constexpr int kStreamKMinKBlocks = 16;             // stream-K: at least this many 128-byte K atoms
 constexpr int64_t kAlignSlack = 1024;                  // dynamic smem is re-aligned to 1024 B
 constexpr int kDefaultRasterGroup = 8;                 // m blocks per raster group (least DRAM traffic on GB300)
 // 512-wide tiles with at least 32 m blocks: groups of 16 read less from DRAM
@@ -384,22 +383,6 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
         if (cg == 2 && !mn_a && !mn_b && !(d.flags & GEMM_FLAG_STAGE_K2) && d.N >= 1024 &&
             (pad512 - pad256) * 20 <= d.N)
             tile_n = 512;
-        // ... unless their waves leave much of the grid idle while 256-wide tiles
-        // can spread a partial last wave over every pair with stream-K: 4096^3
-        // bf16 is 128 512-wide tiles, 84 % of two waves of 76 pairs, and runs
-        // 3 % faster as 256-wide tiles with stream-K on GB300; 8192^3 fills
-        // 96 % of its waves and stays 512-wide (14 % faster than 256-wide).
-        if (tile_n == 512) {
-            int64_t clusters = props.sm_count / cg;
-            if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
-            const int64_t m_blocks = ceil_div(d.M, 128 * cg);
-            const int64_t tiles512 = m_blocks * ceil_div(d.N, 512) * d.batch;
-            const int64_t tiles256 = m_blocks * ceil_div(d.N, 256) * d.batch;
-            const bool sk256 = !(d.flags & (GEMM_FLAG_NO_STREAM_K | GEMM_FLAG_ACCUM_F16)) && clusters >= 2 &&
-                               ceil_div(d.K, 128 / elem_bytes(d.dtype_a)) >= kStreamKMinKBlocks &&
-                               tiles256 >= clusters && tiles256 % clusters != 0;
-            if (sk256 && 10 * tiles512 < 9 * ceil_div(tiles512, clusters) * clusters) tile_n = 256;
-        }
     }
     // 512-wide tiles: two N = 256 MMAs per K step into one 512-column
     // accumulator (K-major operands, one K atom per stage)
@@ -559,8 +542,8 @@ bool encode_sf_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kq, i
 // Stream-K for the 16-bit persistent kernel: when the tiles do not fill whole
 // waves of clusters, the last wave plus one full wave (sk_tiles >= clusters)
 // are split evenly along K over all clusters; the rest stays data-parallel.
-// Worth it only for long K (the fixup moves one fp32 tile per split;
-// kStreamKMinKBlocks).
+// Worth it only for long K (the fixup moves one fp32 tile per split).
+constexpr int kStreamKMinKBlocks = 16;   // 128-byte K atoms
 
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
     info->stream_k_tiles = 0;

@@ -303,9 +303,7 @@ def test_full_square8192_bf16_f32_256x256_pair_tiles_integers_bit_exact():
 
 @pytest.mark.slow
 def test_full_square4096_bf16_bf16_integers_bit_exact():
-    # 128 512-wide tiles would fill 84 % of two waves: the planner takes 256-wide
-    # tiles with stream-K over the partial last wave (partials exact in fp32 too)
-    check_sampled_exact("square4096_bf16", "bf16", expect={"cta_group": 2, "tile_n": 256, "stream_k_tiles": 104})
+    check_sampled_exact("square4096_bf16", "bf16", expect={"cta_group": 2, "tile_n": 512})
 
 
 @pytest.mark.slow
