@@ -159,6 +159,39 @@ def test_wide_tiles_split_schedule_bit_exact(cg_flag, max_ctas, K):
     assert r["ok"], (r, info)
 
 
+def test_wide_tiles_stream_k_and_split_integers_bit_exact():
+    """One launch with both kinds of 512-wide units: the stream-K region's
+    partial units run every stage on both halves, the data-parallel whole
+    tiles after them run the split schedule.  Integer inputs: every partial
+    sum, the fp32 fix-up included, is exact."""
+    prob = inputs.make("square8192_bf16", M=4096, N=5120, K=2048, dist="ints", seed=78)
+    got, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=512)
+    assert info["tile_n"] == 512 and 0 < info["stream_k_tiles"] < info["num_tiles"], info
+    r = compare(got, dref, s, "f32", TOL_TF32, exact=True)
+    if not r["ok"]:
+        dump_on_failure("wide_sk_split", got=got, dref=dref, sabs=s)
+    assert r["ok"], (r, info)
+
+
+def test_wide_tiles_batched_split_integers_bit_exact():
+    """512-wide split tiles across batch entries (3 x 512 x 1024 x 2048)."""
+    prob = inputs.make("square8192_bf16", M=512, N=1024, K=2048, batch=3, dist="ints", seed=79)
+    wl = prob.wl
+    A, B = prob.A.cuda(), prob.B.cuda()
+    D = torch.full((wl.batch, wl.M, wl.N), float("nan"), device="cuda")
+    desc = dg.make_desc(wl.M, wl.N, wl.K, batch=wl.batch, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32,
+                        flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=512)
+    with dg.Plan(desc) as plan:
+        plan.run(A, B, D)
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, (dg.gemm_status_string(s), rec.role)
+        info = plan.info.as_dict()
+    assert info["tile_n"] == 512
+    dref, sabs = oracle.gemm(prob.A, prob.B, M=wl.M, N=wl.N, K=wl.K, batch=wl.batch, dtype_a="bf16", dtype_b="bf16")
+    r = compare(D.double().cpu().numpy(), dref, sabs, "f32", TOL_TF32, exact=True)
+    assert r["ok"], (r, info)
+
+
 @pytest.mark.parametrize("epi", [dg.GEMM_FLAG_EPILOGUE_TMA, dg.GEMM_FLAG_EPILOGUE_DIRECT])
 def test_wide_tiles_stream_k_random(epi):
     """512-wide pair tiles with stream-K (sampled rows of every tile row band)."""
