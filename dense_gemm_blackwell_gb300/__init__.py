@@ -81,7 +81,8 @@ class GemmPlanInfo(ctypes.Structure):
 class GemmWorkUnit(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int32), ("batch", ctypes.c_int32), ("m_block", ctypes.c_int32),
                 ("n_block", ctypes.c_int32), ("k_block_begin", ctypes.c_int32), ("k_block_end", ctypes.c_int32),
-                ("role", ctypes.c_int32), ("slot", ctypes.c_int32)]
+                ("role", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("slot_first", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

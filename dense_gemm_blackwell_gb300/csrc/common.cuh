@@ -116,10 +116,11 @@ struct PersistentParams {
     uint32_t l2_hints;        // bit 0: A loads evict_last; bit 1: D stores evict_first
     uint64_t timeout_ns;
     // Stream-K: the last sk_tiles tiles of the raster are split into equal K
-    // ranges over all clusters and processed first.  A contributor (the part
-    // of a tile that starts at K block 0) leaves its fp32 partial in
+    // ranges over all clusters and processed first.  A contributor (a part of
+    // a tile that does not end it) leaves its fp32 partial in
     // sk_partials[slot] and publishes sk_flags = the launch's epoch; the
-    // finisher (the part that ends the tile) adds it before storing D.
+    // finisher (the part that ends the tile) adds every contributor's
+    // partial before storing D.
     int32_t sk_tiles;
     // Epilogue without shared-memory staging: each thread writes its row's
     // 128-byte chunks straight to D (frees the staging area for a ring stage).

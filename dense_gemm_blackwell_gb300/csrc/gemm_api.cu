@@ -173,14 +173,20 @@ constexpr int kFp8Threads = 384;
 constexpr int kFp8DefaultTileN = 256;           // planner default for block-scaled problems
 constexpr int64_t kFp8StagingBytes = 8 * 32 * 128;
 
+constexpr int64_t kPairMinKAtoms = 96;   // 128-byte K atoms (K >= 6144 for 16-bit inputs)
+
 int choose_cta_group(const gemm_desc_t& d, const gemm_device_props_t& props, int64_t tile_n) {
     if (d.flags & GEMM_FLAG_CTA_GROUP_1) return 1;
     if (d.flags & GEMM_FLAG_CTA_GROUP_2) return 2;
     // An SM pair halves each SM's B traffic from L2, which pays on long K
     // (measured on GB300: +10 % at 4096^3 and 8192^3).  With short K
-    // (batched 256^3) the loads are HBM-bound and single-SM tiles win.
+    // (batched 256^3) the loads are HBM-bound and single-SM tiles win.  With
+    // fewer pair tiles than pairs both forms occupy the same SMs; there pairs
+    // won from K = 6144 on (bf16: +3 to +16 %), were even at 4096 and lost
+    // at 2048 (-6 %).
     const int64_t pair_tiles = ceil_div(d.M, 256) * ceil_div(d.N, tile_n) * d.batch;
-    return (d.M > 128 && d.K >= 1024 && pair_tiles >= props.sm_count / 2) ? 2 : 1;
+    const int64_t k_atoms = ceil_div(d.K, 128 / elem_bytes(d.dtype_a));
+    return (d.M > 128 && d.K >= 1024 && (pair_tiles >= props.sm_count / 2 || k_atoms >= kPairMinKAtoms)) ? 2 : 1;
 }
 
 gemm_status_t plan_fp8(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
@@ -319,6 +325,26 @@ gemm_status_t plan_mx(const gemm_desc_t& d, const gemm_device_props_t& props, ge
 
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info);
 
+// 512-wide tiles only from this many 128-byte K atoms on (K >= 3072 for 16-bit inputs)
+constexpr int64_t kWideMinKAtoms = 48;
+// Fewer output tiles than clusters: split each tile along K into s ranges on
+// s clusters, so that the otherwise idle SMs share the tiles' K loops.  The
+// finisher of a tile adds the other s - 1 clusters' fp32 partials, which
+// costs about as much as a short K loop: on GB300 (bf16, 128 x 256 tiles) a
+// range pays for its fix-up from 32 K atoms on (512^2 x 8192: 4 ranges of 32
+// beat 8 of 16 by 14 %), and an uneven spread of about 1.2 clusters per tile
+// (64 tiles on 76 pairs, 128 on 152 SMs) ran 12-13 % slower than no split.
+// So s = min(clusters / tiles, K atoms / 32, 8), whole ranges per tile, and
+// no split below two.
+constexpr int64_t kSplitMinKAtoms = 32;
+constexpr int64_t kMaxSplit = 8;
+
+int64_t few_tile_split(const gemm_desc_t& d, int64_t tiles, int64_t k_atoms, int64_t clusters) {
+    if (tiles >= clusters || (d.flags & (GEMM_FLAG_NO_STREAM_K | GEMM_FLAG_ACCUM_F16))) return 1;
+    const int64_t s = std::min(std::min(clusters / tiles, k_atoms / kSplitMinKAtoms), kMaxSplit);
+    return s >= 2 ? s : 1;
+}
+
 gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_plan_info_t* info) {
     std::memset(info, 0, sizeof(*info));
     if (d.dtype_d != GEMM_F32 && d.dtype_d != GEMM_BF16 && d.dtype_d != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
@@ -378,10 +404,16 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
         // SM pairs on long K take 512-wide tiles: each SM then loads 48 instead of
         // 64 bytes of operands per 1024 MMA cycles, which its TMA path sustains
         // (8192^3 bf16 on GB300: 20 % fewer cycles), unless they pad N more
-        // than 256-wide tiles do or the operands are MN-major.
+        // than 256-wide tiles do or the operands are MN-major.  On short K the
+        // single accumulator's drain, once per tile, costs more than that
+        // saves (K <= 2048 bf16 on GB300: 2-34 % slower than 256-wide tiles),
+        // and with tiles for fewer than half of the pairs the narrower tiles
+        // keep more SMs busy (2048^2 x 8192: 28 % faster).
         const int64_t pad256 = round_up(d.N, 256) - d.N, pad512 = round_up(d.N, 512) - d.N;
+        const int64_t k_atoms = ceil_div(d.K, 128 / elem_bytes(d.dtype_a));
+        const int64_t wide_tiles = ceil_div(d.M, 256) * ceil_div(d.N, 512) * d.batch;
         if (cg == 2 && !mn_a && !mn_b && !(d.flags & GEMM_FLAG_STAGE_K2) && d.N >= 1024 &&
-            (pad512 - pad256) * 20 <= d.N)
+            (pad512 - pad256) * 20 <= d.N && k_atoms >= kWideMinKAtoms && wide_tiles >= props.sm_count / 4)
             tile_n = 512;
     }
     // 512-wide tiles: two N = 256 MMAs per K step into one 512-column
@@ -445,8 +477,10 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
     const int64_t tiles = num_m * num_n * d.batch;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     int64_t clusters = props.sm_count / cg;
+    clusters = std::min<int64_t>(clusters, tiles * few_tile_split(d, tiles, ceil_div(d.K, atom_k), clusters));
+    // the cap applies to the grid as planned: below tiles x splits it leaves
+    // ranges that straddle tiles, which the schedule handles as well
     if (d.max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(d.max_ctas / cg, 1));
-    clusters = std::min<int64_t>(clusters, tiles);
 
     info->kernel = GEMM_KERNEL_PERSISTENT;
     info->cta_group = cg;
@@ -539,27 +573,37 @@ bool encode_sf_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kq, i
     return r == CUDA_SUCCESS;
 }
 
-// Stream-K for the 16-bit persistent kernel: when the tiles do not fill whole
-// waves of clusters, the last wave plus one full wave (sk_tiles >= clusters)
-// are split evenly along K over all clusters; the rest stays data-parallel.
-// Worth it only for long K (the fixup moves one fp32 tile per split).
-constexpr int kStreamKMinKBlocks = 16;   // 128-byte K atoms
+// Stream-K for the 16-bit persistent kernel.  When the tiles do not fill
+// whole waves of clusters, the last wave plus one full wave (sk_tiles >=
+// clusters) are split evenly along K over all clusters; the rest stays
+// data-parallel.  Worth it only for long K: the fix-up moves one fp32 tile
+// per split (K <= 2048 bf16 on GB300 ran 2-15 % slower with it).  With fewer
+// tiles than clusters (the planner then sizes the grid by few_tile_split),
+// every tile is split, over several clusters each.
+constexpr int kStreamKMinKBlocks = 48;   // 128-byte K atoms
 
 void plan_stream_k(const gemm_desc_t& d, gemm_plan_info_t* info) {
     info->stream_k_tiles = 0;
     info->workspace_bytes = 0;
     if (info->kernel != GEMM_KERNEL_PERSISTENT || (d.flags & (GEMM_FLAG_NO_STREAM_K | GEMM_FLAG_ACCUM_F16))) return;
     const int64_t clusters = info->grid / info->cta_group;
-    // the threshold counts 128-byte K atoms, whatever the stage depth
-    const int64_t atoms = std::max<int64_t>(info->tile_k * elem_bytes(d.dtype_a) / 128, 1);
-    const int64_t nk = ceil_div(d.K, info->tile_k) * atoms;
-    if (clusters < 2 || nk < kStreamKMinKBlocks || info->num_tiles < clusters) return;
-    const int64_t rem = info->num_tiles % clusters;
-    if (rem == 0) return;
-    // 512-wide tiles: a partial is 256 KB per CTA to write and add back;
-    // worth it only when the last wave would leave most clusters idle
-    if (info->tile_n > 256 && 2 * rem >= clusters) return;
-    info->stream_k_tiles = (int32_t)(clusters + rem);
+    if (clusters < 2) return;
+    if (info->num_tiles < clusters) {
+        // every range holds at least one K block (few_tile_split keeps a cluster's share >= kSplitMinKAtoms)
+        if (info->num_tiles * ceil_div(d.K, info->tile_k) < clusters) return;
+        info->stream_k_tiles = (int32_t)info->num_tiles;
+    } else {
+        // the threshold counts 128-byte K atoms, whatever the stage depth
+        const int64_t atoms = std::max<int64_t>(info->tile_k * elem_bytes(d.dtype_a) / 128, 1);
+        const int64_t nk = ceil_div(d.K, info->tile_k) * atoms;
+        if (nk < kStreamKMinKBlocks) return;
+        const int64_t rem = info->num_tiles % clusters;
+        if (rem == 0) return;
+        // 512-wide tiles: a partial is 256 KB per CTA to write and add back;
+        // worth it only when the last wave would leave most clusters idle
+        if (info->tile_n > 256 && 2 * rem >= clusters) return;
+        info->stream_k_tiles = (int32_t)(clusters + rem);
+    }
     // one partial slot per cluster: cta_group CTAs x 128 rows x tile_n fp32, plus a flag per epilogue warp
     const int64_t partial_bytes = clusters * info->cta_group * 128 * info->tile_n * 4;
     const int64_t flag_bytes = round_up(clusters * info->cta_group * kSkFlagsPerCta * 4, 256);
@@ -790,8 +834,11 @@ gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_
     p.sk_tiles = info->kernel == GEMM_KERNEL_PERSISTENT ? info->stream_k_tiles : 0;
     // info must be this desc's plan: the tile count and the stream-K region
     // have to agree with the shape, or the raster arithmetic is meaningless
+    // (a region narrower than the grid only as every tile, with a K block per cluster at least)
     if (info->num_tiles != (int64_t)p.tiles_per_batch * std::max<int64_t>(desc->batch, 1) || p.sk_tiles < 0 ||
-        p.sk_tiles > p.num_tiles || (p.sk_tiles > 0 && p.sk_tiles < clusters))
+        p.sk_tiles > p.num_tiles ||
+        (p.sk_tiles > 0 && p.sk_tiles < clusters &&
+         (p.sk_tiles != p.num_tiles || (int64_t)p.num_tiles * p.num_k_blocks < clusters)))
         return GEMM_ERR_INVALID_ARG;
     gemm_work_unit_t r{};
     r.tile = -1;
@@ -807,6 +854,7 @@ gemm_status_t gemm_plan_work_unit(const gemm_desc_t* desc, const gemm_plan_info_
         r.k_block_end = u.kb1;
         r.role = u.role;
         r.slot = u.role == dgb::kUnitWhole ? 0 : u.slot;
+        r.slot_first = u.role == dgb::kUnitFinisher ? u.slot0 : r.slot;
     }
     *out = r;
     return GEMM_OK;
@@ -1339,10 +1387,11 @@ gemm_status_t gemm_run_noalloc(const gemm_desc_t* desc, const void* A, const voi
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
     p.props.cc_minor = v;
     if (p.props.cc_major != 10 || p.props.cc_minor != 3) return GEMM_ERR_NO_DEVICE;
+    r.d.flags |= GEMM_FLAG_NO_STREAM_K;   // no workspace here: data-parallel tiles only, one cluster per tile at most
     s = plan(r.d, p.props, &p.info);
     if (s != GEMM_OK) return s;
     if ((s = cap_resident(r.d, &p.info)) != GEMM_OK) return s;
-    p.info.stream_k_tiles = 0;      // no workspace here: data-parallel tiles only
+    p.info.stream_k_tiles = 0;
     p.info.workspace_bytes = 0;
     void* record = nullptr;
     if ((s = noalloc_address(dev, &record)) != GEMM_OK) return s;

@@ -421,8 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             auto release_all = [&]() {
                 for (int q = 0; q < parts; ++q) release(q);
             };
-            const size_t part_base = (size_t)(u.slot * CG + (int)rank) * 128 * p.tile_n / 4;   // in float4
-            uint32_t* flag = p.sk_flags + (u.slot * CG + (int)rank) * kEpilogueWarps + half * 4 + wq;
+            // slot s's partial of this CTA (in float4) and this warp's flag of it
+            auto part_base_of = [&](int s) { return (size_t)(s * CG + (int)rank) * 128 * p.tile_n / 4; };
+            auto flag_of = [&](int s) { return p.sk_flags + (s * CG + (int)rank) * kEpilogueWarps + half * 4 + wq; };
+            const size_t part_base = part_base_of(u.slot);
+            uint32_t* flag = flag_of(u.slot);
 
             if (u.role == kUnitContributor) {
                 // Leave this K range's fp32 partial for the finisher, then publish it.
@@ -461,18 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
             const bool adds = u.role == kUnitFinisher;
             bool staged = false;    // partial gathered into this warp's slice of the ring
             if (adds) {
-                int got = 0;
+                // the tile's contributors: slots u.slot (the latest K range) down to u.slot0
+                int got = 1;
                 if (lane == 0)
-                    got = wait_flag(flag, sk_launch_epoch(p.sk_epoch), abort_flag, tmo, p.status, kRoleEpilogue,
-                                    u.slot, t);
+                    for (int s = u.slot; s >= u.slot0 && got; --s)
+                        got = wait_flag(flag_of(s), sk_launch_epoch(p.sk_epoch), abort_flag, tmo, p.status,
+                                        kRoleEpilogue, s, t);
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     release_all();
                     break;
                 }
-                uint32_t v;   // every lane acquires the flag before reading the partial
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-                (void)v;
+                for (int s = u.slot; s >= u.slot0; --s) {
+                    uint32_t v;   // every lane acquires the flags before reading the partials
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag_of(s)) : "memory");
+                    (void)v;
+                }
                 // A finisher is its cluster's last unit: with its accumulator
                 // full, no copy or MMA touches the operand ring again, so the
                 // partial is gathered there by asynchronous copies (a whole part
@@ -533,19 +540,24 @@ __global__ void __launch_bounds__(kThreads, 1) persistent_kernel(const __grid_co
                         if (cc >= nc) break;
                         const int c = c0 + cc;
                         if (adds) {
+                            // own part (later K) + the contributors' partials, latest K range first:
+                            // one fixed order
+                            for (int sl = u.slot; sl >= u.slot0; --sl) {
+                                const bool from_slice = staged && sl == u.slot;
+                                const float4* ps = reinterpret_cast<const float4*>(p.sk_partials) + part_base_of(sl);
 #pragma unroll
-                            for (int h = 0; h < kSub; ++h) {
+                                for (int h = 0; h < kSub; ++h) {
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    const float4 qv =
-                                        staged ? slice_f4[(((c - c_lo) * kSub + h) * 8 + j) * 32 + lane]
-                                               : __ldcg(part + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
-                                    // own part (later K) + partial (earlier K): one fixed order
-                                    const int q = cc * kSub + h;
-                                    r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);
-                                    r[q][4 * j + 1] = __float_as_uint(__uint_as_float(r[q][4 * j + 1]) + qv.y);
-                                    r[q][4 * j + 2] = __float_as_uint(__uint_as_float(r[q][4 * j + 2]) + qv.z);
-                                    r[q][4 * j + 3] = __float_as_uint(__uint_as_float(r[q][4 * j + 3]) + qv.w);
+                                    for (int j = 0; j < 8; ++j) {
+                                        const float4 qv =
+                                            from_slice ? slice_f4[(((c - c_lo) * kSub + h) * 8 + j) * 32 + lane]
+                                                       : __ldcg(ps + sk_partial_index(p.tile_n, wq, c * kSub + h, j, lane));
+                                        const int q = cc * kSub + h;
+                                        r[q][4 * j] = __float_as_uint(__uint_as_float(r[q][4 * j]) + qv.x);
+                                        r[q][4 * j + 1] = __float_as_uint(__uint_as_float(r[q][4 * j + 1]) + qv.y);
+                                        r[q][4 * j + 2] = __float_as_uint(__uint_as_float(r[q][4 * j + 2]) + qv.z);
+                                        r[q][4 * j + 3] = __float_as_uint(__uint_as_float(r[q][4 * j + 3]) + qv.w);
+                                    }
                                 }
                             }
                         }

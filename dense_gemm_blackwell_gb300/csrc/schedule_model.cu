@@ -132,18 +132,21 @@ gemm_status_t gemm_plan_schedule(const gemm_desc_t* desc, const gemm_plan_info_t
         return GEMM_ERR_INVALID_ARG;
     const int64_t clusters = info->grid / info->cta_group;
     const int64_t k_slices = (desc->K + info->tile_k - 1) / info->tile_k;
+    int64_t k_run = k_slices;   // K slices the model runs per tile
     int64_t tiles = (info->num_tiles + clusters - 1) / clusters;
     if (info->stream_k_tiles > 0) {
-        // a cluster's share of all K slices, counted in whole tiles
+        // a cluster's share of all K slices, counted in whole tiles, or as
+        // one shorter tile when it is less than a tile (fewer tiles than clusters)
         const int64_t slices = (info->num_tiles * k_slices + clusters - 1) / clusters;
         tiles = (slices + k_slices - 1) / k_slices;
+        if (slices < k_slices) k_run = slices;
     }
-    if (tiles > (1 << 20) || k_slices > (1 << 20) || tiles * k_slices > (1 << 24)) return GEMM_ERR_UNSUPPORTED;
+    if (tiles > (1 << 20) || k_run > (1 << 20) || tiles * k_run > (1 << 24)) return GEMM_ERR_UNSUPPORTED;
     // tf32 multiplies at half the 16-bit rate (nominal 1.1 against 2.25 PFLOP/s)
     const double rate = mc.mma_flops_per_cycle * (desc->dtype_a == GEMM_TF32 ? 0.5 : 1.0);
     gemm_sched_params_t p{};
     p.tiles = (int32_t)tiles;
-    p.k_slices = (int32_t)k_slices;
+    p.k_slices = (int32_t)k_run;
     p.stages = info->stages;
     p.accumulators = info->tmem_stages;
     const double stage_bytes = (double)info->stage_bytes;   // per CTA, A and B

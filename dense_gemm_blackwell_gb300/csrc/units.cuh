@@ -31,18 +31,25 @@ struct WorkUnit {
     int tile;
     int kb0, kb1;
     int role;    // kUnitWhole, kUnitContributor or kUnitFinisher
-    int slot;    // partial slot written (contributor) or read (finisher)
+    int slot;    // partial slot written (contributor) or the last one read (finisher)
+    int slot0;   // finisher: the first partial slot read; it adds slots slot, slot-1, ..., slot0
 };
 constexpr int kUnitWhole = 0, kUnitContributor = 1, kUnitFinisher = 2;
 
 // The idx-th unit of cluster c (of G) in processing order.
 //  1. Stream-K region (tiles [T - sk_tiles, T)): its sk_tiles * nk K blocks
-//     are cut into G contiguous ranges, one per cluster.  Each range is at
-//     least one tile long (sk_tiles >= G), so a tile is split between at most
-//     two clusters: c-1 holds its start (contributor, slot c-1) and c its end
-//     (finisher).  A cluster walks its range from the last segment to the
+//     are cut into G contiguous ranges, one per cluster, and each range into
+//     segments at tile boundaries.  A segment that ends its tile but does not
+//     start it is a finisher; one that does not end its tile is a contributor
+//     and leaves its fp32 partial in slot c (only a range's last segment can
+//     be one); the rest are whole tiles.  With ranges at least one tile long
+//     (sk_tiles >= G) a tile is split between clusters c-1 and c.  With fewer
+//     tiles than clusters (sk_tiles == T < G) ranges are shorter, and the
+//     contributors of a tile are all the clusters slot0 .. c-1 before its
+//     finisher c.  A cluster walks its range from the last segment to the
 //     first: it publishes its contributor partial before anything else and
-//     reaches its finisher segment last, when c-1's partial is long done.
+//     reaches its finisher segment last, so a finisher waits only on
+//     clusters that wait on no one.
 //  2. Data-parallel tiles c, c+G, ... of [0, T - sk_tiles).  Run after the
 //     stream-K region, they hide a finisher's fix-up behind the MMAs of the
 //     cluster's next tile; without them the finisher is the cluster's last
@@ -63,8 +70,11 @@ __host__ __device__ __forceinline__ bool next_unit(const PersistentParams& p, in
                 u.kb0 = (int)(lo - j * nk);
                 u.kb1 = (int)(hi - j * nk);
                 const bool starts = u.kb0 == 0, ends = u.kb1 == nk;
-                u.role = (starts && ends) ? kUnitWhole : (starts ? kUnitContributor : kUnitFinisher);
-                u.slot = starts ? c : c - 1;
+                u.role = ends ? (starts ? kUnitWhole : kUnitFinisher) : kUnitContributor;
+                u.slot = ends ? (starts ? 0 : c - 1) : c;
+                // the cluster whose range holds the tile's first K block:
+                // the largest c0 with floor(total * c0 / G) <= j * nk
+                u.slot0 = (u.role == kUnitFinisher) ? (int)(((j * nk + 1) * G + total - 1) / total - 1) : u.slot;
                 return true;
             }
             ++k;
@@ -79,6 +89,7 @@ __host__ __device__ __forceinline__ bool next_unit(const PersistentParams& p, in
     u.kb1 = nk;
     u.role = kUnitWhole;
     u.slot = 0;
+    u.slot0 = 0;
     return true;
 }
 

@@ -159,7 +159,7 @@ typedef struct {
     int64_t stage_bytes;     /* bytes of one ring stage per CTA */
     int64_t pipeline_bytes;  /* ring + 8 B per barrier (2 per stage, 2 per TMEM stage) + 4 B TMEM handle */
     int64_t smem_bytes;      /* dynamic shared memory per CTA, all included */
-    int32_t stream_k_tiles;  /* tiles whose K range is split between two clusters (0 = data-parallel only) */
+    int32_t stream_k_tiles;  /* tiles whose K range is split between clusters (0 = data-parallel only) */
     int32_t epilogue;        /* 0 = TMA stores through shared-memory staging, 1 = direct row stores */
     int64_t workspace_bytes; /* device scratch the plan holds for stream-K partials and flags */
 } gemm_plan_info_t;
@@ -217,8 +217,10 @@ typedef struct {
     int32_t k_block_begin;   /* contraction range [k_block_begin * tile_k, k_block_end * tile_k), */
     int32_t k_block_end;     /* clipped to K */
     int32_t role;            /* 0 whole tile; 1 stream-K contributor (leaves an fp32 partial);
-                                2 stream-K finisher (adds that partial and writes D) */
-    int32_t slot;            /* partial slot written (role 1) or read (role 2); 0 for role 0 */
+                                2 stream-K finisher (adds the tile's partials and writes D) */
+    int32_t slot;            /* partial slot written (role 1), or the last one read (role 2); 0 for role 0 */
+    int32_t slot_first;      /* role 2: the first slot read -- the finisher adds the partials of slots
+                                slot, slot - 1, ..., slot_first in that order; otherwise equal to slot */
 } gemm_work_unit_t;
 
 /*
@@ -229,8 +231,9 @@ typedef struct {
  * arithmetic only, touching no GPU: the same schedule functions the kernels
  * run, compiled for the host, so a caller can check which tiles and K ranges
  * each SM (pair) takes.  Order: first the stream-K region's segments (the last
- * wave plus one full wave, cut into equal K ranges, each cluster walking its
- * range from the end), then data-parallel tiles, raster groups of m blocks
+ * wave plus one full wave, or every tile when there are fewer tiles than
+ * clusters, cut into equal K ranges, each cluster walking its range from the
+ * end), then data-parallel tiles, raster groups of m blocks
  * first (the L2 reuse across a wave that the "Hopper and Blackwell GEMM" page
  * asks for next to its table of ridges).  The block-scaled kernel has no
  * stream-K region (its producers call the same functions; its MMA and

@@ -218,7 +218,7 @@ def test_stream_k_plan():
     """Tiles that do not fill whole waves: the last wave plus one full wave are
     split along K (stream-K), one fp32 partial slot per cluster."""
     for kw in (dict(M=8192, N=8192, K=8192, tile_n=256),      # 1024 tiles over 76 pairs
-               dict(M=2048, N=5120, K=2048)):                 # 80 512-wide tiles: the last wave holds 4
+               dict(M=2048, N=5120, K=4096)):                 # 80 512-wide tiles: the last wave holds 4
         s, info = query(dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, **kw)
         assert s == dg.GEMM_OK
         clusters = info.grid // info.cta_group
@@ -228,8 +228,9 @@ def test_stream_k_plan():
     # 512-wide tiles with a last wave at least half full stay data-parallel
     s, info = query(M=8192, N=8192, K=8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
     assert s == dg.GEMM_OK and info.tile_n == 512 and info.stream_k_tiles == 0
-    # whole waves, short K, or the flag: data-parallel only, no workspace
+    # whole waves, short K (under 48 K atoms), or the flag: data-parallel only, no workspace
     for kw in (dict(M=256 * 76, N=256, K=8192), dict(M=256, N=256, K=256, batch=512),
+               dict(M=8192, N=8192, K=2048, tile_n=256),
                dict(M=8192, N=8192, K=8192, flags=dg.GEMM_FLAG_NO_STREAM_K)):
         s, info = query(dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, **kw)
         assert s == dg.GEMM_OK and info.stream_k_tiles == 0 and info.workspace_bytes == 0, kw

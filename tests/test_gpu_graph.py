@@ -82,7 +82,7 @@ def test_stream_k_graph_replays_new_data():
         assert info["kernel"] == dg.GEMM_KERNEL_PERSISTENT and info["stream_k_tiles"] > 0, info
     # 80 pair tiles of 256 x 256 on 76 clusters: every tile is split along K
     replay_and_check("square8192_bf16", "f32", 5, 60, expect,
-                     flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_STAGE_K2, M=2048, N=2560, K=2048)
+                     flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_STAGE_K2, M=2048, N=2560, K=4096)
 
 
 def test_graph_replay_is_cheaper_than_a_call():

@@ -66,7 +66,7 @@ def test_mn_major_integers_bit_exact(cg_flag, mn_a, mn_b):
 
 @pytest.mark.parametrize("out", ["bf16", "f16"])
 def test_mn_major_random_16bit_out_and_stream_k(out):
-    prob = inputs.make("square4096_bf16", M=1024, N=1024, K=2048, seed=82)
+    prob = inputs.make("square4096_bf16", M=1024, N=1024, K=4096, seed=82)
     got, dref, s, info = run_mn(prob, out, True, True, flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
     assert info["stream_k_tiles"] > 0
     assert compare(got, dref, s, out, TOL_16BIT)["ok"]

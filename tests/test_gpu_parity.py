@@ -127,7 +127,7 @@ def test_persistent_ragged(cg_flag, dtype_in, out):
 @pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
 def test_epilogue_modes_ragged(mode, out):
     """Direct row stores and TMA-staged stores write the same D, ragged edges included."""
-    prob = inputs.make("square8192_bf16", M=600, N=712, K=1088, dist="ints", seed=19)
+    prob = inputs.make("square8192_bf16", M=600, N=712, K=3136, dist="ints", seed=19)
     r, info = check_full(prob, out, exact=True, flags=dg.GEMM_FLAG_CTA_GROUP_2 | mode)
     assert info["epilogue"] == (1 if mode == dg.GEMM_FLAG_EPILOGUE_DIRECT else 0)
     r, info = check_full(prob, out, exact=True, flags=dg.GEMM_FLAG_CTA_GROUP_2 | mode, max_ctas=8)
@@ -148,10 +148,10 @@ def test_persistent_few_ctas_many_tiles():
 
 
 @pytest.mark.parametrize("cg_flag,M,N,K,ctas,out", [
-    (dg.GEMM_FLAG_CTA_GROUP_2, 1024, 1024, 1024, 10, "f32"),
-    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 704, 1040, 8, "bf16"),
-    (dg.GEMM_FLAG_CTA_GROUP_1, 640, 768, 1152, 7, "f32"),
-    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 2064, 4, "f16"),
+    (dg.GEMM_FLAG_CTA_GROUP_2, 1024, 1024, 3072, 10, "f32"),
+    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 704, 3088, 8, "bf16"),
+    (dg.GEMM_FLAG_CTA_GROUP_1, 640, 768, 3200, 7, "f32"),
+    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 4112, 4, "f16"),
 ])
 def test_stream_k_integers_bit_exact(cg_flag, M, N, K, ctas, out):
     """Capping the clusters forces a partial last wave: its tiles are split
@@ -162,8 +162,8 @@ def test_stream_k_integers_bit_exact(cg_flag, M, N, K, ctas, out):
 
 
 @pytest.mark.parametrize("cg_flag,M,N,K,ctas,out", [
-    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 1000, 1040, 16, "f32"),   # 12 tiles on 8 pairs
-    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 2064, 8, "bf16"),    # 15 tiles on 8 CTAs
+    (dg.GEMM_FLAG_CTA_GROUP_2, 600, 1000, 3088, 16, "f32"),   # 12 tiles on 8 pairs
+    (dg.GEMM_FLAG_CTA_GROUP_1, 520, 600, 4112, 8, "bf16"),    # 15 tiles on 8 CTAs
 ])
 def test_stream_k_only_ragged_bit_exact(cg_flag, M, N, K, ctas, out):
     """Every tile in the stream-K region, so each finisher is its cluster's
@@ -175,7 +175,7 @@ def test_stream_k_only_ragged_bit_exact(cg_flag, M, N, K, ctas, out):
 
 
 def test_stream_k_matches_data_parallel():
-    prob = inputs.make("square4096_bf16", M=1024, N=768, K=2048, seed=18)
+    prob = inputs.make("square4096_bf16", M=1024, N=768, K=4096, seed=18)
     D1, info1 = run_gpu(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, max_ctas=10)
     D2, info2 = run_gpu(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_NO_STREAM_K, max_ctas=10)
     assert info1["stream_k_tiles"] > 0 and info2["stream_k_tiles"] == 0

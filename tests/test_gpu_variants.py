@@ -106,7 +106,7 @@ def test_two_atom_stages_bit_exact(cg_flag, dtype_in, K):
 def test_two_atom_stages_stream_k_random():
     """Stream-K splits count K blocks of the deeper stage (sampled rows of
     every tile row band against the oracle)."""
-    prob = inputs.make("square8192_bf16", M=2048, N=2560, K=2048, seed=74)
+    prob = inputs.make("square8192_bf16", M=2048, N=2560, K=4096, seed=74)
     wl = prob.wl
     A, B = prob.A.cuda(), prob.B.cuda()
     D = torch.full((wl.M, wl.N), float("nan"), device="cuda")
@@ -164,7 +164,7 @@ def test_wide_tiles_stream_k_and_split_integers_bit_exact():
     partial units run every stage on both halves, the data-parallel whole
     tiles after them run the split schedule.  Integer inputs: every partial
     sum, the fp32 fix-up included, is exact."""
-    prob = inputs.make("square8192_bf16", M=4096, N=5120, K=2048, dist="ints", seed=78)
+    prob = inputs.make("square8192_bf16", M=4096, N=5120, K=4096, dist="ints", seed=78)
     got, dref, s, info = run(prob, "f32", flags=dg.GEMM_FLAG_CTA_GROUP_2, tile_n=512)
     assert info["tile_n"] == 512 and 0 < info["stream_k_tiles"] < info["num_tiles"], info
     r = compare(got, dref, s, "f32", TOL_TF32, exact=True)
@@ -195,7 +195,7 @@ def test_wide_tiles_batched_split_integers_bit_exact():
 @pytest.mark.parametrize("epi", [dg.GEMM_FLAG_EPILOGUE_TMA, dg.GEMM_FLAG_EPILOGUE_DIRECT])
 def test_wide_tiles_stream_k_random(epi):
     """512-wide pair tiles with stream-K (sampled rows of every tile row band)."""
-    prob = inputs.make("square8192_bf16", M=2048, N=5120, K=2048, seed=76)
+    prob = inputs.make("square8192_bf16", M=2048, N=5120, K=4096, seed=76)
     wl = prob.wl
     A, B = prob.A.cuda(), prob.B.cuda()
     D = torch.full((wl.M, wl.N), float("nan"), device="cuda")

@@ -7,11 +7,13 @@ rest on:
 
 * every (tile, K block) pair is computed exactly once;
 * tile indices map one to one onto (batch, m block, n block) inside D;
-* a tile split along K (stream-K) has one contributor, K blocks [0, x), and
-  one finisher, [x, nk), in neighbouring clusters c-1 and c, which share the
-  contributor's partial slot c-1; the contributor is the first unit of its
-  cluster and the finisher the last of its cluster's stream-K units, so a
-  finisher never waits on a cluster that is itself waiting;
+* a tile split along K (stream-K) is held by consecutive clusters c0 .. c:
+  contributors (K blocks [0, x1), [x1, x2), ...) in c0 .. c-1, each writing
+  its own partial slot, and the finisher (the tile's last K blocks) in c,
+  which reads slots c-1 down to c0; with ranges at least one tile long that
+  is one contributor, c-1.  A contributor is the first unit of its cluster
+  and a finisher the last of its cluster's stream-K units, so a finisher
+  never waits on a cluster that is itself waiting;
 * clusters get equal shares: data-parallel tiles differ by at most one, and
   stream-K ranges by at most one K block;
 * raster groups: a wave's tiles walk m blocks first inside a group.
@@ -88,15 +90,24 @@ def check_schedule(desc, info, group=None):
         if len(parts) == 1:
             c, i, u = parts[0]
             assert u["role"] == 0 and (u["k_block_begin"], u["k_block_end"]) == (0, nk)
+            assert u["slot"] == u["slot_first"] == 0
             continue
-        assert sk > 0 and t >= T - sk and len(parts) == 2, (t, parts)
-        (c0, i0, u0), (c1, i1, u1) = sorted(parts, key=lambda p: p[2]["k_block_begin"])
-        assert u0["role"] == 1 and u1["role"] == 2, (u0, u1)
-        assert u0["k_block_end"] == u1["k_block_begin"]
-        assert c1 == c0 + 1 and u0["slot"] == u1["slot"] == c0
-        assert i0 == 0, "a contributor publishes before its cluster does anything else"
-        n_sk = sum(1 for u in sched[c1] if u["tile"] >= T - sk)
-        assert i1 == n_sk - 1, "a finisher is its cluster's last stream-K unit"
+        assert sk > 0 and t >= T - sk, (t, parts)
+        if sk >= G:
+            assert len(parts) == 2, (t, parts)
+        parts = sorted(parts, key=lambda p: p[2]["k_block_begin"])
+        c0 = parts[0][0]
+        for n, (c, i, u) in enumerate(parts):
+            assert c == c0 + n, "a tile's parts sit in consecutive clusters"
+            if n:
+                assert u["k_block_begin"] == parts[n - 1][2]["k_block_end"]
+            if n + 1 < len(parts):
+                assert u["role"] == 1 and u["slot"] == u["slot_first"] == c, u
+                assert i == 0, "a contributor publishes before its cluster does anything else"
+            else:
+                assert u["role"] == 2 and u["slot"] == c - 1 and u["slot_first"] == c0, u
+                n_sk = sum(1 for v in sched[c] if v["tile"] >= T - sk)
+                assert i == n_sk - 1, "a finisher is its cluster's last stream-K unit"
 
     # balance
     dp = [sum(1 for u in lst if u["tile"] < T - sk) for lst in sched.values()]
@@ -105,7 +116,10 @@ def check_schedule(desc, info, group=None):
         kbs = [sum(u["k_block_end"] - u["k_block_begin"] for u in lst if u["tile"] >= T - sk)
                for lst in sched.values()]
         assert max(kbs) - min(kbs) <= 1 and sum(kbs) == sk * nk
-        assert min(kbs) >= nk, "every stream-K range is at least one tile long"
+        if sk >= G:
+            assert min(kbs) >= nk, "every stream-K range is at least one tile long"
+        else:
+            assert sk == T and min(kbs) >= 1, "fewer tiles than clusters: every tile split, no empty range"
 
     # raster: inside a group, consecutive tiles step m first
     if group:
@@ -139,10 +153,78 @@ def test_stream_k_region_256_wide():
 
 def test_stream_k_only():
     """80 tiles of 256 x 512 on 76 pairs: every tile is in the stream-K region."""
-    desc, info = plan(2048, 5120, 2048, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, tile_n=512)
+    desc, info = plan(2048, 5120, 4096, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32, tile_n=512)
     assert info.stream_k_tiles == info.num_tiles == 80
     sched = check_schedule(desc, info)
     assert all(u["tile"] >= 0 for lst in sched.values() for u in lst)
+
+
+@pytest.mark.parametrize("M,N,K,kw,tiles,grid,most_parts", [
+    (128, 8192, 8192, {}, 32, 128, 4),        # 32 tiles: 4 ranges of 32 K atoms each
+    (512, 512, 8192, {}, 4, 32, 4),           # long K: 4 pair tiles, 4 ranges each
+    (512, 512, 8192, {"flags": dg.GEMM_FLAG_CTA_GROUP_1}, 8, 32, 4),
+    (64, 64, 65536, {}, 1, 8, 8),             # one tile: 8 ranges (the cap)
+    (256, 256, 16384, {}, 1, 16, 8),
+    (1024, 2048, 8192, {"flags": dg.GEMM_FLAG_CTA_GROUP_2, "tile_n": 512}, 16, 128, 4),   # 16 pair tiles
+    # a cap below tiles x splits: ranges straddle tiles, middle contributors
+    (128, 2048, 4096, {"max_ctas": 13}, 8, 13, 3),
+    (200, 1000, 4160, {"max_ctas": 11}, 8, 11, 3),
+])
+def test_few_tiles_split_along_k(M, N, K, kw, tiles, grid, most_parts):
+    """Fewer tiles than clusters: the grid grows past the tile count and every
+    tile is split along K, several clusters per tile, one finisher each."""
+    desc, info = plan(M, N, K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, **kw)
+    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (tiles, grid, tiles)
+    sched = check_schedule(desc, info)
+    parts = {}
+    for lst in sched.values():
+        for u in lst:
+            parts[u["tile"]] = parts.get(u["tile"], 0) + 1
+    assert max(parts.values()) == most_parts
+    assert all(lst for lst in sched.values()), "no cluster idles"
+    if "max_ctas" not in kw:
+        assert len(set(parts.values())) == 1, "equal ranges per tile"
+
+
+@pytest.mark.parametrize("M,N,K", [(8192, 1024, 8192), (1024, 8192, 8192), (2048, 2048, 8192)])
+def test_near_full_wave_not_split(M, N, K):
+    """Tiles for more than half of the clusters: an uneven spread (about 1.2
+    clusters per tile) measured slower than none, so the grid stays one
+    cluster per tile."""
+    desc, info = plan(M, N, K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    assert info.stream_k_tiles == 0 and info.grid == info.num_tiles * info.cta_group
+
+
+def test_residency_cap_leaves_uneven_ranges():
+    """A grid smaller than tiles x splits (as a residency cap can leave it):
+    the schedule still covers every K block once, with ranges across tiles."""
+    desc, info = plan(512, 512, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    for G in (9, 13, 31):
+        capped = dg.GemmPlanInfo.from_buffer_copy(info)
+        capped.grid = G * info.cta_group
+        check_schedule(desc, capped)
+
+
+def test_few_tiles_short_k_and_opt_out_stay_data_parallel():
+    # 16 K atoms per tile: too short to split
+    desc, info = plan(128, 8192, 1024, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (32, 32, 0)
+    check_schedule(desc, info)
+    desc, info = plan(128, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, flags=dg.GEMM_FLAG_NO_STREAM_K)
+    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (32, 32, 0)
+    desc, info = plan(512, 512, 8192, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F16, flags=dg.GEMM_FLAG_ACCUM_F16)
+    assert info.stream_k_tiles == 0 and info.grid == info.num_tiles * info.cta_group
+
+
+@pytest.mark.parametrize("K,tile_n,sk", [(1024, 256, 0), (2048, 256, 0), (3072, 512, 0), (4096, 512, 0)])
+def test_short_k_tile_width_and_stream_k(K, tile_n, sk):
+    """Short K: 256-wide pair tiles (two accumulators) rather than 512-wide, and
+    no stream-K region until a tile holds 48 K atoms."""
+    desc, info = plan(8192, 8192, K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    assert (info.cta_group, info.tile_n, info.stream_k_tiles) == (2, tile_n, sk)
+    desc, info = plan(8192, 8192, K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, tile_n=256)
+    assert info.stream_k_tiles == (0 if K < 3072 else 76 + 1024 % 76)
+    check_schedule(desc, info)
 
 
 def test_batched_and_block_scaled():
@@ -197,8 +279,12 @@ def test_argument_errors():
     zero_n = dg.make_desc(8192, 0, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
     assert dg.gemm_plan_work_unit(zero_n, info, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
     bad_sk = dg.GemmPlanInfo.from_buffer_copy(info)
-    bad_sk.stream_k_tiles = 5                      # fewer than the 76 clusters
+    bad_sk.stream_k_tiles = 5                      # fewer than the 76 clusters, and not every tile
     assert dg.gemm_plan_work_unit(desc, bad_sk, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
+    # every tile split, but fewer K blocks than clusters: some range would be empty
+    desc1, info1 = plan(64, 64, 65536, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    few = dg.make_desc(64, 64, 64 * 7, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    assert dg.gemm_plan_work_unit(few, info1, 0, 0)[0] == dg.GEMM_ERR_INVALID_ARG
     desc, info = plan(128, 64, 64, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F32)
     assert info.kernel == dg.GEMM_KERNEL_SINGLE_CTA
     assert dg.gemm_plan_work_unit(desc, info, 0, 0)[0] == dg.GEMM_ERR_UNSUPPORTED
