@@ -415,6 +415,13 @@ gemm_status_t plan(const gemm_desc_t& d, const gemm_device_props_t& props, gemm_
         if (cg == 2 && !mn_a && !mn_b && !(d.flags & GEMM_FLAG_STAGE_K2) && d.N >= 1024 &&
             (pad512 - pad256) * 20 <= d.N && k_atoms >= kWideMinKAtoms && wide_tiles >= props.sm_count / 4)
             tile_n = 512;
+        // 256-wide tiles for fewer than half of the clusters: 128-wide tiles
+        // occupy twice the SMs before any split along K, and a split's fix-up
+        // is the kernel's tail (bf16 on GB300: 10-35 % faster on 14 such
+        // shapes from 128 x 8192 x 8192 to 1536^2 x 6144; from two thirds of
+        // the clusters on, 256-wide tiles were faster again).
+        const int64_t tiles256 = ceil_div(d.M, 128 * cg) * ceil_div(d.N, 256) * d.batch;
+        if (tile_n == 256 && 2 * tiles256 < props.sm_count / cg) tile_n = 128;
     }
     // 512-wide tiles: two N = 256 MMAs per K step into one 512-column
     // accumulator (K-major operands, one K atom per stage)

@@ -74,8 +74,9 @@ CASES = [
     (64, 64, 65536, "f32", 1, {}),
     (256, 256, 16384, "bf16", 1, {}),
     (128, 2048, 4096, "bf16", 1, {}),
-    (128, 2048, 4096, "f32", 1, {"max_ctas": 13}),
-    (200, 1000, 4160, "f16", 1, {"max_ctas": 11}),
+    (128, 2048, 4096, "bf16", 1, {"tile_n": 256}),
+    (128, 2048, 4096, "f32", 1, {"max_ctas": 13, "tile_n": 256}),
+    (200, 1000, 4160, "f16", 1, {"max_ctas": 11, "tile_n": 256}),
     (1024, 2048, 8192, "f32", 1, {"flags": dg.GEMM_FLAG_CTA_GROUP_2, "tile_n": 512}),
     (512, 768, 6144, "bf16", 1, {"flags": dg.GEMM_FLAG_CTA_GROUP_2, "tile_n": 256}),
     (128, 256, 8192, "f32", 3, {}),

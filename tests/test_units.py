@@ -160,15 +160,17 @@ def test_stream_k_only():
 
 
 @pytest.mark.parametrize("M,N,K,kw,tiles,grid,most_parts", [
-    (128, 8192, 8192, {}, 32, 128, 4),        # 32 tiles: 4 ranges of 32 K atoms each
-    (512, 512, 8192, {}, 4, 32, 4),           # long K: 4 pair tiles, 4 ranges each
-    (512, 512, 8192, {"flags": dg.GEMM_FLAG_CTA_GROUP_1}, 8, 32, 4),
+    (128, 8192, 8192, {}, 64, 128, 2),        # 64 tiles 128 wide: 2 ranges of 64 K atoms each
+    (512, 512, 8192, {}, 8, 64, 4),           # long K: 8 pair tiles 128 wide, 4 ranges each
+    (128, 8192, 8192, {"tile_n": 256}, 32, 128, 4),
+    (512, 512, 8192, {"tile_n": 256}, 4, 32, 4),
+    (512, 512, 8192, {"flags": dg.GEMM_FLAG_CTA_GROUP_1, "tile_n": 256}, 8, 32, 4),
     (64, 64, 65536, {}, 1, 8, 8),             # one tile: 8 ranges (the cap)
-    (256, 256, 16384, {}, 1, 16, 8),
+    (256, 256, 16384, {"tile_n": 256}, 1, 16, 8),
     (1024, 2048, 8192, {"flags": dg.GEMM_FLAG_CTA_GROUP_2, "tile_n": 512}, 16, 128, 4),   # 16 pair tiles
     # a cap below tiles x splits: ranges straddle tiles, middle contributors
-    (128, 2048, 4096, {"max_ctas": 13}, 8, 13, 3),
-    (200, 1000, 4160, {"max_ctas": 11}, 8, 11, 3),
+    (128, 2048, 4096, {"max_ctas": 13, "tile_n": 256}, 8, 13, 3),
+    (200, 1000, 4160, {"max_ctas": 11, "tile_n": 256}, 8, 11, 3),
 ])
 def test_few_tiles_split_along_k(M, N, K, kw, tiles, grid, most_parts):
     """Fewer tiles than clusters: the grid grows past the tile count and every
@@ -184,6 +186,16 @@ def test_few_tiles_split_along_k(M, N, K, kw, tiles, grid, most_parts):
     assert all(lst for lst in sched.values()), "no cluster idles"
     if "max_ctas" not in kw:
         assert len(set(parts.values())) == 1, "equal ranges per tile"
+
+
+@pytest.mark.parametrize("M,N,K,cg,tile_n", [
+    (128, 8192, 8192, 1, 128), (256, 4096, 4096, 1, 128), (1536, 1536, 6144, 2, 128), (512, 512, 8192, 2, 128),
+    (3000, 1000, 4000, 1, 256), (2048, 2048, 8192, 2, 256), (2048, 2048, 2048, 1, 256), (8192, 8192, 8192, 2, 512),
+])
+def test_default_tile_width(M, N, K, cg, tile_n):
+    """256-wide tiles for fewer than half of the clusters narrow to 128."""
+    desc, info = plan(M, N, K, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    assert (info.cta_group, info.tile_n) == (cg, tile_n)
 
 
 @pytest.mark.parametrize("M,N,K", [(8192, 1024, 8192), (1024, 8192, 8192), (2048, 2048, 8192)])
@@ -208,10 +220,10 @@ def test_residency_cap_leaves_uneven_ranges():
 def test_few_tiles_short_k_and_opt_out_stay_data_parallel():
     # 16 K atoms per tile: too short to split
     desc, info = plan(128, 8192, 1024, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
-    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (32, 32, 0)
+    assert (info.tile_n, info.num_tiles, info.grid, info.stream_k_tiles) == (128, 64, 64, 0)
     check_schedule(desc, info)
     desc, info = plan(128, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, flags=dg.GEMM_FLAG_NO_STREAM_K)
-    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (32, 32, 0)
+    assert (info.num_tiles, info.grid, info.stream_k_tiles) == (64, 64, 0)
     desc, info = plan(512, 512, 8192, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F16, flags=dg.GEMM_FLAG_ACCUM_F16)
     assert info.stream_k_tiles == 0 and info.grid == info.num_tiles * info.cta_group
 
