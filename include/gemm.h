@@ -416,8 +416,9 @@ typedef struct {
  * and a machine's unit costs (NULL: the GB300 figures this library measured,
  * see gemm_machine_gb300) it derives, per SM (pair):
  *   tiles      T = ceil(output tiles / clusters) (stream-K plans: the K slices of
- *                  one cluster's share, in whole tiles)
- *   k_slices   K = ceil(K / tile_k)
+ *                  one cluster's share, in whole tiles, or 1 when that share is
+ *                  less than a tile)
+ *   k_slices   K = ceil(K / tile_k) (a share less than a tile: its K slices)
  *   t_mma      = 2 * 128 * tile_n * tile_k / mma rate
  *   t_issue    = stage_fixed + stage_bytes / ingest      (the copy path's throughput)
  *   t_load     = load_latency + stage_bytes / ingest     (one stage's data in)

@@ -139,6 +139,26 @@ def test_plan_schedule_finds_the_load_bound_shape():
     assert min(range(3), key=lambda i: out[i][1]) == 1
 
 
+def test_plan_schedule_few_tiles_runs_one_share():
+    """Fewer tiles than clusters: each cluster runs one K range of one tile,
+    so the model runs a single tile of that range's K slices; a stream-K plan
+    with ranges of a tile or more still counts whole tiles."""
+    props = dg.GemmDeviceProps(**GB300)
+    desc = dg.make_desc(512, 512, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16)
+    st, info = dg.gemm_plan_query(desc, props)
+    assert st == dg.GEMM_OK and 0 < info.stream_k_tiles == info.num_tiles < info.grid // info.cta_group
+    st, p, r, _, _ = dg.gemm_plan_schedule(desc, info, props)
+    assert st == dg.GEMM_OK
+    k_slices = -(-8192 // info.tile_k)
+    clusters = info.grid // info.cta_group
+    assert p.tiles == 1 and p.k_slices == -(-info.num_tiles * k_slices // clusters) < k_slices
+    desc = dg.make_desc(8192, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_BF16, tile_n=256)
+    st, info = dg.gemm_plan_query(desc, props)
+    assert st == dg.GEMM_OK and info.stream_k_tiles >= info.grid // info.cta_group
+    st, p, r, _, _ = dg.gemm_plan_schedule(desc, info, props)
+    assert p.k_slices == -(-8192 // info.tile_k) and p.tiles == 14   # 1024 tiles over 76 pairs: 13.5 -> 14
+
+
 def test_plan_schedule_rejects_what_it_does_not_model():
     props = dg.GemmDeviceProps(**GB300)
     desc = dg.make_desc(4096, 4096, 4096, dtype_a=dg.GEMM_E4M3, dtype_d=dg.GEMM_BF16,
