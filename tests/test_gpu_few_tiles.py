@@ -121,3 +121,47 @@ def test_few_tiles_opt_out_matches():
     assert info["stream_k_tiles"] > 0 and info1["stream_k_tiles"] == 0
     assert info1["grid"] == info1["num_tiles"] * info1["cta_group"]
     assert (split[0] == whole[0]).all() and (split[0] == oracle.round_to("f32", dref)).all()
+
+
+def test_few_tiles_split_tf32_integers_bit_exact():
+    """fp32 storage at tf32 precision (32-element K atoms): small integers are
+    exact, so the split product equals the oracle bit for bit."""
+    M, N, K = 128, 1024, 4096
+    g = torch.Generator().manual_seed(94)
+    A = torch.randint(-3, 4, (M, K), generator=g).float()
+    B = torch.randint(-3, 4, (N, K), generator=g).float()
+    desc = dg.make_desc(M, N, K, dtype_a=dg.GEMM_TF32, dtype_d=dg.GEMM_F32)
+    D = torch.full((M, N), float("nan"), device="cuda")
+    with dg.Plan(desc) as plan:
+        info = plan.info.as_dict()
+        plan.run(A.cuda(), B.cuda(), D)
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, dg.gemm_status_string(s)
+    assert info["stream_k_tiles"] == info["num_tiles"] < info["grid"] // info["cta_group"], info
+    dref, sabs = oracle.gemm(A, B, M=M, N=N, K=K, dtype_a="f32", dtype_b="f32")
+    r = compare(D.double().cpu().numpy(), dref, sabs, "f32", 4e-3, exact=True)
+    assert r["ok"], (r, info)
+
+
+@pytest.mark.parametrize("mn_a,mn_b", [(True, False), (False, True), (True, True)])
+def test_few_tiles_split_mn_major_f16_bit_exact(mn_a, mn_b):
+    """MN-major operands (stored [k][m] / [k][n]) on split tiles, f16 in and out."""
+    M, N, K = 256, 512, 8192
+    prob = inputs.make("square8192_bf16", M=M, N=N, K=K, dist="ints", seed=95, dtype_in="f16")
+    A, B = prob.A, prob.B
+    As = A.t().contiguous() if mn_a else A
+    Bs = B.t().contiguous() if mn_b else B
+    desc = dg.make_desc(M, N, K, dtype_a=dg.GEMM_F16, dtype_d=dg.GEMM_F16,
+                        major_a=dg.GEMM_MN_MAJOR if mn_a else dg.GEMM_K_MAJOR,
+                        major_b=dg.GEMM_MN_MAJOR if mn_b else dg.GEMM_K_MAJOR)
+    D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    with dg.Plan(desc) as plan:
+        info = plan.info.as_dict()
+        plan.run(As.cuda(), Bs.cuda(), D)
+        s, rec = plan.sync_status()
+        assert s == dg.GEMM_OK, dg.gemm_status_string(s)
+    assert info["stream_k_tiles"] == info["num_tiles"] < info["grid"] // info["cta_group"], info
+    dref, sabs = oracle.gemm(As, Bs, M=M, N=N, K=K, dtype_a="f16", dtype_b="f16",
+                             major_a="mn" if mn_a else "k", major_b="mn" if mn_b else "k")
+    r = compare(D.double().cpu().numpy(), dref, sabs, "f16", TOL_16BIT, exact=True)
+    assert r["ok"], (r, info)

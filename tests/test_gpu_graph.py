@@ -85,6 +85,18 @@ def test_stream_k_graph_replays_new_data():
                      flags=dg.GEMM_FLAG_CTA_GROUP_2 | dg.GEMM_FLAG_STAGE_K2, M=2048, N=2560, K=4096)
 
 
+def test_few_tiles_split_graph_replays_new_data():
+    """Fewer tiles than clusters: each finisher adds several clusters' partials,
+    each waited for by its flag.  Five replays of one capture on new inputs,
+    each bit-exact: no finisher took a previous replay's partial."""
+    def expect(info):
+        clusters = info["grid"] // info["cta_group"]
+        assert info["kernel"] == dg.GEMM_KERNEL_PERSISTENT, info
+        assert info["stream_k_tiles"] == info["num_tiles"] and clusters >= 4 * info["num_tiles"], info
+    # 512 x 512 x 8192: 8 pair tiles of 256 x 128, each split four ways
+    replay_and_check("square8192_bf16", "bf16", 5, 70, expect, M=512, N=512, K=8192)
+
+
 def test_graph_replay_is_cheaper_than_a_call():
     """Replaying a captured small problem costs the host less than calling
     gemm_run through the binding (the launch-bound case graphs are for):
