@@ -277,6 +277,34 @@ def test_random_shapes():
         n += 1
 
 
+def test_random_few_tile_shapes():
+    """Seeded skinny and long-K shapes, so that most plans split tiles over
+    several clusters: the split count stays within 2..8, each range keeps at
+    least 32 K atoms (16-bit: 64-element atoms), the grid never exceeds the
+    SMs, and the whole schedule passes the invariants above."""
+    rng = random.Random(11)
+    split = 0
+    for _ in range(60):
+        M = rng.choice([1, 64, 100, 128, 256, 384, 512, 1024])
+        N = rng.choice([64, 128, 200, 512, 1000, 2048, 4096, 8192])
+        K = rng.choice([2048, 4096, 6000, 8192, 16384, 65536])
+        kw = dict(dtype_a=rng.choice([dg.GEMM_BF16, dg.GEMM_F16]), dtype_d=rng.choice([dg.GEMM_F32, dg.GEMM_BF16]),
+                  flags=dg.GEMM_FLAG_NO_SINGLE_CTA)
+        desc = dg.make_desc(M, N, K, **kw)
+        s, info = dg.gemm_plan_query(desc, GB300)
+        assert s == dg.GEMM_OK, (M, N, K)
+        G = info.grid // info.cta_group
+        assert info.grid <= GB300.sm_count and info.grid % info.cta_group == 0
+        if 0 < info.stream_k_tiles == info.num_tiles < G:
+            split += 1
+            s_per_tile = G // info.num_tiles
+            assert G == s_per_tile * info.num_tiles and 2 <= s_per_tile <= 8, (M, N, K, info.as_dict())
+            atoms = -(-K // 64)
+            assert atoms // s_per_tile >= 32, (M, N, K, s_per_tile)
+        check_schedule(desc, info)
+    assert split >= 20, split
+
+
 def test_argument_errors():
     desc, info = plan(8192, 8192, 8192, dtype_a=dg.GEMM_BF16, dtype_d=dg.GEMM_F32)
     G = info.grid // info.cta_group
